@@ -1,0 +1,144 @@
+"""fp64 CPU oracle for the sparse MLA attention forward (test infrastructure).
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package.  The product path (the CUDA library and its
+binding) never does, and this package imports nothing from the product.
+
+The arithmetic lives in ``smla_oracle.c`` (plain C, fp64); this module builds
+it with gcc and marshals numpy arrays to it.  The C file's header gives the
+definition it follows and the pages it cites.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "smla_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libsmla_oracle.so")
+_lib = None
+_lock = threading.Lock()
+
+KV_BF16 = 0
+KV_E4M3 = 1
+KV_E4M3_GROUP128 = 2
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into a shared library (no fast-math, no FMA
+    contraction, so the arithmetic is the C source's)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+           "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        lib.smla_oracle_fwd.restype = ctypes.c_int
+        lib.smla_oracle_fwd.argtypes = [
+            P, P, ctypes.c_int, P, P, P, ctypes.c_int64, ctypes.c_int,
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+            ctypes.c_double, P, ctypes.c_int64, P, P, ctypes.c_int]
+        lib.smla_oracle_merge.restype = None
+        lib.smla_oracle_merge.argtypes = [P, P, ctypes.c_int, ctypes.c_int64,
+                                          ctypes.c_int, P, P]
+        lib.smla_oracle_e4m3_to_f64.restype = ctypes.c_double
+        lib.smla_oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        lib.smla_oracle_bf16_to_f64.restype = ctypes.c_double
+        lib.smla_oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        _lib = lib
+        return lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def e4m3_to_f64(byte: int) -> float:
+    return _load().smla_oracle_e4m3_to_f64(int(byte))
+
+
+def bf16_to_f64(bits: int) -> float:
+    return _load().smla_oracle_bf16_to_f64(int(bits))
+
+
+def default_threads() -> int:
+    return os.cpu_count() or 1
+
+
+def sparse_mla_fwd(q_bits, kv, kv_dtype, k_scale, indices, valid_len,
+                   sm_scale, d_v=512, num_slots=None, tokens=None,
+                   n_threads=None):
+    """Oracle forward.
+
+    q_bits    uint16 [T, h, d_qk]  (bf16 bit patterns)
+    kv        uint16 [S, d_qk] (bf16 bits) or uint8 [S, d_qk] (E4M3 bytes)
+    kv_dtype  KV_BF16 / KV_E4M3 / KV_E4M3_GROUP128
+    k_scale   float32 [1] or [S, ceil(d_qk/128)] or None
+    indices   int32 [T, topk];  valid_len int32 [T] or None
+    tokens    optional int64 list of token ids (rows of the result follow it)
+    Returns (O float64 [n, h, d_v], LSE float64 [n, h]).
+    """
+    lib = _load()
+    q_bits = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    T, h, d_qk = q_bits.shape
+    want = np.uint16 if kv_dtype == KV_BF16 else np.uint8
+    kv = np.ascontiguousarray(kv, dtype=want).reshape(-1, d_qk)
+    S = kv.shape[0] if num_slots is None else int(num_slots)
+    indices = np.ascontiguousarray(indices, dtype=np.int32)
+    assert indices.shape[0] == T
+    topk = indices.shape[1]
+    if valid_len is not None:
+        valid_len = np.ascontiguousarray(valid_len, dtype=np.int32)
+        assert valid_len.shape == (T,)
+    if k_scale is not None:
+        k_scale = np.ascontiguousarray(k_scale, dtype=np.float32)
+    if tokens is not None:
+        tokens = np.ascontiguousarray(tokens, dtype=np.int64)
+        n = tokens.shape[0]
+    else:
+        n = T
+    out = np.zeros((n, h, d_v), dtype=np.float64)
+    lse = np.zeros((n, h), dtype=np.float64)
+    rc = lib.smla_oracle_fwd(
+        _ptr(q_bits), _ptr(kv), int(kv_dtype), _ptr(k_scale), _ptr(indices),
+        _ptr(valid_len), T, h, d_qk, int(d_v), topk, S, float(sm_scale),
+        _ptr(tokens), n, _ptr(out), _ptr(lse),
+        int(n_threads or default_threads()))
+    if rc != 0:
+        raise RuntimeError(f"smla_oracle_fwd failed with code {rc}")
+    return out, lse
+
+
+def merge(o_parts, lse_parts):
+    """LSE-weighted merge of partial results over disjoint key sets.
+
+    o_parts float64 [P, rows, d_v] (each normalised over its keys),
+    lse_parts float64 [P, rows].  Returns (O [rows, d_v], LSE [rows])."""
+    lib = _load()
+    o_parts = np.ascontiguousarray(o_parts, dtype=np.float64)
+    lse_parts = np.ascontiguousarray(lse_parts, dtype=np.float64)
+    P, rows, d_v = o_parts.shape
+    assert lse_parts.shape == (P, rows)
+    out = np.zeros((rows, d_v), dtype=np.float64)
+    lse = np.zeros((rows,), dtype=np.float64)
+    lib.smla_oracle_merge(_ptr(o_parts), _ptr(lse_parts), P, rows, d_v,
+                          _ptr(out), _ptr(lse))
+    return out, lse

@@ -1,0 +1,40 @@
+"""Test-side glue: hand a generated workload to the oracle as numpy arrays."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+
+def bits16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def kv_numpy(w) -> np.ndarray:
+    if w.kv.dtype == torch.bfloat16:
+        return bits16(w.kv)
+    return w.kv.detach().contiguous().cpu().numpy()
+
+
+def oracle_fwd(w, tokens=None, valid=True, n_threads=None, indices=None):
+    """Run the oracle on workload `w` (optionally a token subset)."""
+    ks = None if w.k_scale is None else w.k_scale.detach().cpu().numpy()
+    idx = (w.indices if indices is None else indices).detach().cpu().numpy()
+    vl = w.valid_len.detach().cpu().numpy() if valid else None
+    return oracle.sparse_mla_fwd(bits16(w.q), kv_numpy(w), w.kv_dtype, ks, idx,
+                                 vl, w.sm_scale, d_v=w.d_v,
+                                 num_slots=w.num_slots, tokens=tokens,
+                                 n_threads=n_threads)
+
+
+def dequant_rows_torch(w) -> torch.Tensor:
+    """float64 [S, d_qk] dequantized cache via torch's own dtype casts (a
+    library route independent of the oracle's decoder)."""
+    if w.kv.dtype == torch.bfloat16:
+        return w.kv.cpu().to(torch.float64)
+    x = w.kv.cpu().view(torch.float8_e4m3fn).to(torch.float64)
+    if w.kv_dtype == 1:
+        return x * float(w.k_scale.cpu()[0])
+    grp = torch.arange(w.d_qk) // 128
+    return x * w.k_scale.cpu().to(torch.float64)[:, grp]
