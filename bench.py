@@ -1,0 +1,486 @@
+"""Benchmark of the sparse MLA attention forward on GB300.
+
+One step = one smla_fwd_ws call over the whole workload (every step of the hot
+path: work setup, gather, dequant, QK^T, softmax, PV, epilogue, and the
+combine when the plan splits the top-k range) with inputs resident in HBM.
+
+Headline workload: the bf16 prefill shape — one 8192-token sequence, h=128
+heads, d_qk=576, d_v=512, topk=2048, token i selecting min(i+1, 2048)
+distinct slots of [0, i] — the h=128 / topk=2048 case whose compute roofline
+is the tensor cores.  The decode shape (T=64, h=128, topk=2048, 2 M-slot bf16
+pool) is reported beside it under "secondary".
+
+Metric: TFLOP/s with FLOPs = sum_t 2 * h * v_t * (d_qk + d_v) over the actual
+valid counts v_t, plus query-tokens/s; `value` is the whole-job TFLOP/s over
+all ranks.  N > 1 (torchrun): every rank runs its own copy of the workload
+(independent problems, no data-path collective), so scaling is weak.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from sparse_mla_attention_02_gb300 import workloads as W  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                  "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+METRIC = ("sparse MLA fwd TFLOP/s & query-tokens/s at h=128 topk=2048; "
+          "% of roofline")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def flops_of(w) -> float:
+    v = w.valid_len.to(torch.float64).clamp(0, w.topk)
+    return float(2.0 * w.h * (w.d_qk + w.d_v) * v.sum().item())
+
+
+def row_bytes(w) -> int:
+    return 2 * w.d_qk if w.kv_dtype == W.KV_BF16 else w.d_qk
+
+
+def bytes_model(w):
+    """Algorithmic bytes: per-token terms (q, O, LSE, indices, valid) plus the
+    selected rows once per token (G) or once overall (U)."""
+    G = (w.d_qk + 127) // 128
+    scale_b = 4 * G if w.kv_dtype == W.KV_FP8_E4M3_GROUP128 else 0
+    per_tok = w.T * (2 * w.h * w.d_qk + 2 * w.h * w.d_v + 4 * w.h
+                     + 4 * w.topk + 4)
+    v = w.valid_len.clamp(0, w.topk)
+    gathered = int(v.sum().item()) * (row_bytes(w) + scale_b)
+    mask = torch.arange(w.topk, device=w.indices.device)[None, :] < v[:, None]
+    uniq = int(torch.unique(w.indices[mask & (w.indices >= 0)]).numel())
+    return per_tok + uniq * (row_bytes(w) + scale_b), per_tok + gathered
+
+
+def csrc_digest() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "sparse_mla_attention_02_gb300",
+                                           "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[kernel_key]
+        if e.get("csrc_sha") == csrc_digest():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        if not getattr(self, "lines", None):
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except Exception:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        loaded = [s for s in sm if mx and s >= 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def make(name, device):
+    return W.CONFIGS[name](device=device)
+
+
+def time_steps(fn, steps, stream):
+    """K steps back to back on `stream`, timed with CUDA events there."""
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / 1e3
+
+
+def run_ours(args, rank, world, local_rank):
+    import sparse_mla_attention_02_gb300 as smla
+    import torch.distributed as dist
+    from sparse_mla_attention_02_gb300 import build
+    build.build()
+    smla.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    pk, pk_src = peaks()
+
+    def setup(name, seed_shift):
+        w = W.CONFIGS[name](device=dev, seed=1000 + list(W.CONFIGS).index(name)
+                            + 7919 * seed_shift)
+        n = smla.smla_workspace_size(w.T, w.h, w.d_qk, w.topk, w.kv_dtype)
+        ws = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+        out = torch.empty((w.T, w.h, w.d_v), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((w.T, w.h), dtype=torch.float32, device=dev)
+        return w, ws, out, lse, n
+
+    def step_fn(w, ws, out, lse):
+        def f():
+            smla.smla_fwd_ws(w.q, w.kv, w.kv_dtype, w.k_scale, w.indices,
+                             w.valid_len, w.sm_scale, ws, out=out, lse=lse,
+                             num_slots=w.num_slots, stream=stream)
+        return f
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- headline: bf16 prefill --------------------------------------------
+    w, ws, out, lse, ws_n = setup(args.config, rank)
+    fl = flops_of(w)
+    U, G = bytes_model(w)
+    f = step_fn(w, ws, out, lse)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            f()
+    stream.synchronize()
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as cs:
+        elapsed = time_steps(f, args.steps, stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    clocks = cs.summary()
+    t_max = max_over_ranks(elapsed)
+    ms = 1e3 * t_max / args.steps
+    launches_per_step = 1 + (1 if ws_n > 0 else 0)
+    value = world * fl * args.steps / t_max / 1e12
+    tok_s = world * w.T * args.steps / t_max
+    kernel_s = elapsed / args.steps
+    achieved = fl / kernel_s / 1e12
+    bound_tensor = fl / (pk["bf16_tflops"] * 1e12) >= U / (pk["hbm_gbs"] * 1e9)
+    roof = {
+        "kernel": "smla_fwd main kernel" + (" + combine" if ws_n else ""),
+        "bound": "tensor" if bound_tensor else "hbm",
+        "achieved": round(achieved if bound_tensor else U / kernel_s / 1e9, 3),
+        "peak": pk["bf16_tflops"] if bound_tensor else pk["hbm_gbs"],
+        "unit": "TFLOP/s" if bound_tensor else "GB/s",
+        "peak_source": f"{pk_src} ({'bf16 burst' if bound_tensor else 'copy'})",
+        "traffic": ncu_traffic(args.config),
+        "algorithmic_flops_per_launch": fl,
+        "algorithmic_bytes_per_launch": {"U": U, "G": G},
+    }
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["frac_of_sustained"] = round(achieved / pk["bf16_tflops_sustained"], 4) \
+        if bound_tensor else None
+
+    # ---- e2e: host buffers, copies inside the timed region -----------------
+    h_q = torch.empty(w.q.shape, dtype=w.q.dtype, pin_memory=True)
+    h_q.copy_(w.q)
+    h_idx = torch.empty(w.indices.shape, dtype=torch.int32, pin_memory=True)
+    h_idx.copy_(w.indices)
+    h_vl = torch.empty(w.valid_len.shape, dtype=torch.int32, pin_memory=True)
+    h_vl.copy_(w.valid_len)
+    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    d_q = torch.empty_like(w.q)
+    d_idx = torch.empty_like(w.indices)
+    d_vl = torch.empty_like(w.valid_len)
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            d_q.copy_(h_q, non_blocking=True)
+            d_idx.copy_(h_idx, non_blocking=True)
+            d_vl.copy_(h_vl, non_blocking=True)
+            smla.smla_fwd_ws(d_q, w.kv, w.kv_dtype, w.k_scale, d_idx, d_vl,
+                             w.sm_scale, ws, out=out, lse=lse,
+                             num_slots=w.num_slots, stream=stream)
+            h_out.copy_(out, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+    e2e_step()
+    stream.synchronize()
+    e2e_steps = max(3, args.steps // 2)
+    barrier()
+    e2e_el = max_over_ranks(time_steps(e2e_step, e2e_steps, stream))
+    h2d = h_q.numel() * 2 + h_idx.numel() * 4 + h_vl.numel() * 4
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    e2e = {"value": round(world * fl * e2e_steps / e2e_el / 1e12, 3),
+           "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h,
+           "tokens_per_s": round(world * w.T * e2e_steps / e2e_el, 1),
+           "ms_per_step": round(1e3 * e2e_el / e2e_steps, 3),
+           "resident": "kv cache (model state); q, indices, valid_len copied in, "
+                       "O and LSE copied out each step"}
+    del h_q, h_idx, h_vl, h_out, h_lse, d_q, d_idx, d_vl
+
+    # ---- cpu baseline: the oracle on a bounded sample (rank 0, N=1) ---------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+
+    del w, ws, out, lse
+    torch.cuda.empty_cache()
+
+    # ---- secondary: bf16 decode ----------------------------------------------
+    secondary = {}
+    if not args.no_secondary:
+        for name in ["bf16_decode"]:
+            w2, ws2, out2, lse2, n2 = setup(name, rank)
+            f2 = step_fn(w2, ws2, out2, lse2)
+            with torch.cuda.stream(stream):
+                for _ in range(args.warmup):
+                    f2()
+            stream.synchronize()
+            barrier()
+            k2 = max(args.steps, 20)
+            el2 = max_over_ranks(time_steps(f2, k2, stream))
+            fl2 = flops_of(w2)
+            U2, G2 = bytes_model(w2)
+            t2 = el2 / k2
+            secondary[name] = {
+                "tflops": round(world * fl2 / t2 / 1e12, 3),
+                "tokens_per_s": round(world * w2.T / t2, 1),
+                "ms_per_step": round(1e3 * t2, 4),
+                "hbm_gbs_U": round(U2 / t2 / 1e9, 1),
+                "frac_hbm_U": round(U2 / t2 / 1e9 / pk["hbm_gbs"], 4),
+                "roofline_frac": round(max(fl2 / (pk["bf16_tflops"] * 1e12),
+                                           U2 / (pk["hbm_gbs"] * 1e9)) / t2, 4),
+                "splits_workspace_bytes": n2,
+                "l2": "pool 2.4 GB > L2",
+            }
+            del w2, ws2, out2, lse2
+            torch.cuda.empty_cache()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; shapes and selection structure of the "
+                    "pages' workloads)",
+            "config": {"workload": f"{args.config}: T=8192 h=128 d_qk=576 "
+                                   "d_v=512 topk=2048, valid=min(i+1,2048), "
+                                   "8192-slot bf16 pool",
+                       "T": 8192, "h": 128, "topk": 2048, "kv": "bf16",
+                       "l2": "inputs larger than L2 (q 1.21 GB, O 1.07 GB); "
+                             "the 9.4 MB pool is L2-resident by nature",
+                       "parallelism": f"replicas x{world} (independent problems)"},
+            "tokens_per_s": round(tok_s, 1),
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+            "secondary": secondary,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def _oracle_inputs(sub):
+    q = sub.q.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+    if sub.kv.dtype == torch.bfloat16:
+        kv = sub.kv.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+    else:
+        kv = sub.kv.contiguous().cpu().numpy()
+    ks = None if sub.k_scale is None else sub.k_scale.cpu().numpy()
+    return q, kv, ks, sub.indices.cpu().numpy(), sub.valid_len.cpu().numpy()
+
+
+def oracle_sample_rate(w, seconds, rng_seed=0):
+    """Run the oracle on growing token samples until one takes >= seconds/4,
+    then on a sample sized for ~seconds.  Returns (TFLOP/s, tokens/s, n, s)."""
+    import oracle
+    T = w.T
+    cores = oracle.default_threads()
+    n = max(cores, 8)
+    while True:
+        sel = np.unique(np.linspace(0, T - 1, min(n, T)).astype(np.int64))
+        sub = W.token_subset(w, sel)
+        q, kv, ks, idx, vl = _oracle_inputs(sub)
+        t0 = time.perf_counter()
+        oracle.sparse_mla_fwd(q, kv, sub.kv_dtype, ks, idx, vl, sub.sm_scale,
+                              num_slots=sub.num_slots, n_threads=cores)
+        dt = time.perf_counter() - t0
+        fl = flops_of(sub)
+        if dt >= seconds / 4 or len(sel) >= T:
+            if dt < seconds / 2 and len(sel) < T:
+                n = int(n * min(8.0, seconds / max(dt, 1e-3)))
+                continue
+            return fl / dt / 1e12, len(sel) / dt, len(sel), dt, cores
+        n = int(n * min(8.0, max(2.0, seconds / 4 / max(dt, 1e-3))))
+
+
+def cpu_baseline(w, seconds):
+    """The oracle as it stands (never tuned for this), on the host cores,
+    over an evenly spaced token sample of the same workload sized for about
+    `seconds` of CPU work."""
+    tf, tok, n, dt, cores = oracle_sample_rate(w, seconds)
+    return {"value": round(tf, 6), "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle", "tokens_per_s": round(tok, 3),
+            "sample": f"{n} of {w.T} tokens evenly spaced over the sequence "
+                      f"(all heads, their own valid counts), {dt:.1f} s, fp64 "
+                      f"C oracle on {cores} threads"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is the fp64 CPU oracle on a
+    bounded token sample of the same workload (rank 0 only)."""
+    if rank != 0:
+        return
+    w = W.CONFIGS[args.config](device="cpu", seed=1003)
+    import oracle
+    cores = oracle.default_threads()
+    T = w.T
+    n = args.ref_tokens
+    sel = np.unique(np.linspace(T // 4, T - 1, n).astype(np.int64))
+    sub = W.token_subset(w, sel)
+    q, kv, ks, idx, vl = _oracle_inputs(sub)
+    fl = flops_of(sub)
+
+    def step():
+        oracle.sparse_mla_fwd(q, kv, sub.kv_dtype, ks, idx, vl, sub.sm_scale,
+                              num_slots=sub.num_slots, n_threads=cores)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = fl * args.steps / dt / 1e12
+    sample = (f"{len(sel)} of {T} tokens evenly spaced over the last 3/4 of "
+              f"the sequence per step, fp64 C oracle on {cores} threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6),
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": f"{args.config}: T=8192 h=128 d_qk=576 d_v=512 "
+                               "topk=2048 (token sample, see cpu_baseline)"},
+        "tokens_per_s": round(len(sel) * args.steps / dt, 3),
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s",
+                         "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="bf16_prefill")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-tokens", type=int, default=32)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) \
+            else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

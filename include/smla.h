@@ -1,0 +1,165 @@
+/*
+ * smla.h — C ABI of libsmla: sparse MLA attention forward on GB300 (sm_103a).
+ *
+ * The operation (vLLM "Sparse MLA on Hopper: Use SGLang's kernel for the
+ * sparse mla low latency runs", ops/cutlass_fa3.py, flash_attn_with_kvcache
+ * docstring; vLLM API docs flashmla_sparse, FlashMLASparseImpl; and
+ * flashinfer_mla_sparse_sm90.py, module docstring): for every query token t
+ * and head p, attend only to the token's selected cache slots
+ *
+ *   J_t = { j < min(valid_len[t], topk) : 0 <= indices[t,j] < num_slots }
+ *   s_j = sm_scale * < q[t,p,0:d_qk], K_j >      K_j = dequant(kv[indices[t,j]])
+ *   O[t,p,:] = sum_j softmax(s)_j * K_j[0:d_v]   (V is the d_v-prefix of K)
+ *   LSE[t,p] = ln sum_j exp(s_j)
+ *
+ * with one latent KV row shared by all heads (MQA-like).  A token with no
+ * selected slot gets O = 0 and LSE = -inf (the LSE-merge identity of the
+ * flashmla_sparse page, _forward_fp8_kv_mixed_batch).
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers named as device pointers must be device memory of the current
+ *    device (or managed memory); host pointers are named as such.
+ *  - All buffers are owned by the caller.  The library keeps no pointer past
+ *    a call, except its own lazily grown workspace (smla_fwd only).
+ *  - Work is enqueued on `stream` and returns without synchronising, unless
+ *    a function says otherwise.
+ *  - Arguments are checked on the host before anything is launched; a bad
+ *    argument returns SMLA_ERR_INVALID_ARG or SMLA_ERR_UNSUPPORTED and
+ *    launches nothing.  T = 0 returns SMLA_OK and launches nothing.
+ *  - Device-side conditions (an index >= num_slots, a bounded wait that ran
+ *    out) never fault: the element is masked or the block exits, and a bit is
+ *    set in a device status word that smla_get_device_status reads.
+ */
+#ifndef SMLA_H_
+#define SMLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define SMLA_API __attribute__((visibility("default")))
+#else
+#define SMLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* KV cache element formats.
+ *  SMLA_KV_BF16: bf16 rows of d_qk elements (cutlass_fa3_sparse.py,
+ *    get_kv_cache_shape: 576 bf16 = [kv_c_normed 512 | k_pe 64]).
+ *  SMLA_KV_FP8_E4M3: E4M3 bytes, value = e4m3 * k_scale[0]
+ *    (flashinfer_mla_sparse_sm90.py: per-tensor k_scale, FP8 read directly).
+ *  SMLA_KV_FP8_E4M3_GROUP128: E4M3 bytes, value = e4m3 * k_scale[slot*G + c/128],
+ *    G = ceil(d_qk/128) (the per-token x 128-channel-group ckv_scale_arr). */
+typedef enum {
+  SMLA_KV_BF16 = 0,
+  SMLA_KV_FP8_E4M3 = 1,
+  SMLA_KV_FP8_E4M3_GROUP128 = 2
+} smla_kv_dtype;
+
+typedef enum {
+  SMLA_OK = 0,
+  SMLA_ERR_INVALID_ARG = 1,  /* NULL pointer, bad size, misaligned buffer */
+  SMLA_ERR_UNSUPPORTED = 2,  /* a shape or format the library does not serve */
+  SMLA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+  SMLA_ERR_TIMEOUT = 4,      /* device status: a bounded wait ran out */
+  SMLA_ERR_BAD_INDEX = 5,    /* device status: an index >= num_slots was masked */
+  SMLA_ERR_WORKSPACE = 6     /* the caller's workspace is smaller than needed */
+} smla_status;
+
+/*
+ * smla_fwd — the sparse MLA forward (the whole hot path: work setup, index
+ * gather, FP8 dequant, QK^T, masked online softmax, PV, epilogue, and the
+ * LSE-weighted combine when the top-k range is split across CTAs).
+ *
+ *  q          device, bf16 [T, h, d_qk] contiguous; d_qk = 576 ([nope 512 |
+ *             rope 64]) or 512 (NoPE).  16-byte aligned.
+ *  kv_cache   device, [num_slots, d_qk] contiguous rows: bf16 (2*d_qk bytes a
+ *             row) or E4M3 bytes (d_qk bytes a row).  16-byte aligned.
+ *  kv_dtype   an smla_kv_dtype value.
+ *  k_scale    device fp32: NULL for SMLA_KV_BF16; [1] for SMLA_KV_FP8_E4M3;
+ *             [num_slots, ceil(d_qk/128)] for SMLA_KV_FP8_E4M3_GROUP128.
+ *  indices    device int32 [T, topk]: global slot ids; entries < 0 or
+ *             >= num_slots are masked wherever they sit (the -1 tail, or
+ *             scattered -1 as the flashmla_sparse page's DCP path leaves them).
+ *  valid_len  device int32 [T] (clamped to [0, topk]), or NULL: then every
+ *             entry of the row is considered and masked entries skipped.
+ *  T, h       query tokens (>= 0) and heads (1..128).
+ *  d_v        must be 512.
+ *  topk       index row width (>= 1).
+ *  num_slots  rows in kv_cache (>= 1, < 2^31).
+ *  sm_scale   multiplies the raw dot product (e.g. 1/sqrt(576)).
+ *  out        device, bf16 [T, h, d_v], written in full.  16-byte aligned.
+ *  lse        device fp32 [T, h] natural-log LSE, or NULL to skip it.
+ *  stream     CUDA stream (0 = legacy default stream).
+ *
+ * Uses a library-owned device workspace for split partial results, grown
+ * with cudaMalloc on first need (so the first call of a new, larger shape
+ * allocates); smla_fwd_ws takes a caller-owned workspace instead.
+ */
+SMLA_API smla_status smla_fwd(const void* q, const void* kv_cache, int kv_dtype,
+                     const float* k_scale, const int32_t* indices,
+                     const int32_t* valid_len, int T, int h, int d_qk, int d_v,
+                     int topk, int64_t num_slots, float sm_scale, void* out,
+                     float* lse, cudaStream_t stream);
+
+/*
+ * smla_workspace_size — bytes of device workspace smla_fwd_ws needs for this
+ * shape on the current device (0 when the plan does not split the top-k
+ * range).  Deterministic for a given (shape, device SM count).
+ */
+SMLA_API size_t smla_workspace_size(int T, int h, int d_qk, int d_v, int topk,
+                           int kv_dtype);
+
+/*
+ * smla_fwd_ws — smla_fwd with a caller-owned device workspace of at least
+ * smla_workspace_size(...) bytes (256-byte aligned; NULL allowed when that
+ * size is 0).  Returns SMLA_ERR_WORKSPACE if it is too small.  Performs no
+ * allocation and no host synchronisation.  One workspace must not be shared by
+ * calls that may overlap on the GPU.
+ */
+SMLA_API smla_status smla_fwd_ws(const void* q, const void* kv_cache, int kv_dtype,
+                        const float* k_scale, const int32_t* indices,
+                        const int32_t* valid_len, int T, int h, int d_qk,
+                        int d_v, int topk, int64_t num_slots, float sm_scale,
+                        void* out, float* lse, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * smla_combine — LSE-weighted merge of partial results computed over disjoint
+ * key sets (the split-KV combine, and the cross-rank merge of the
+ * flashmla_sparse page's DCP path):
+ *   LSE = ln sum_p exp(LSE_p)  (-inf parts contribute nothing)
+ *   O   = sum_p exp(LSE_p - LSE) * O_p,   all parts -inf -> (0, -inf)
+ *  o_parts    device fp32 [n_parts, rows, d_v], each part normalised over its keys
+ *  lse_parts  device fp32 [n_parts, rows]
+ *  out        device bf16 [rows, d_v];  lse  device fp32 [rows] or NULL
+ *  d_v        must be 512; n_parts 1..64; rows >= 0.
+ */
+SMLA_API smla_status smla_combine(const float* o_parts, const float* lse_parts,
+                         int n_parts, int64_t rows, int d_v, void* out,
+                         float* lse, cudaStream_t stream);
+
+/*
+ * smla_get_device_status — read (and optionally clear) the current device's
+ * status word: 0, or the SMLA_ERR_TIMEOUT / SMLA_ERR_BAD_INDEX condition
+ * seen first since the last clear.  Synchronises the device; meant for tests
+ * and diagnostics, not the hot path.
+ */
+SMLA_API smla_status smla_get_device_status(int* status_out, int clear);
+
+/* smla_status_string — a static, human-readable name for a status code. */
+SMLA_API const char* smla_status_string(int status);
+
+/* smla_version — library version as major*10000 + minor*100 + patch. */
+SMLA_API int smla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SMLA_H_ */

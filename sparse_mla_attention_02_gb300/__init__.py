@@ -1,1 +1,187 @@
-"""GB300-native sparse MLA attention forward (placeholder; binding follows)."""
+"""GB300-native sparse MLA attention forward.
+
+A thin Python binding over the C ABI of libsmla (include/smla.h): the
+functions below carry the C names, take torch tensors that already live on the
+GPU, check dtypes and shapes, and pass raw pointers and sizes through ctypes.
+Every step of the computation runs in the library's CUDA kernels; there is no
+fallback of any kind.  If libsmla.so has not been built (``build.build()``,
+or ``__graft_entry__.build()``), every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+_lib = None
+_lock = threading.Lock()
+
+SMLA_KV_BF16 = 0
+SMLA_KV_FP8_E4M3 = 1
+SMLA_KV_FP8_E4M3_GROUP128 = 2
+
+SMLA_OK = 0
+STATUS_NAMES = {0: "SMLA_OK", 1: "SMLA_ERR_INVALID_ARG",
+                2: "SMLA_ERR_UNSUPPORTED", 3: "SMLA_ERR_CUDA",
+                4: "SMLA_ERR_TIMEOUT", 5: "SMLA_ERR_BAD_INDEX",
+                6: "SMLA_ERR_WORKSPACE"}
+
+
+class SmlaError(RuntimeError):
+    def __init__(self, code, what):
+        super().__init__(f"{what}: {STATUS_NAMES.get(code, code)}")
+        self.code = code
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load libsmla.so (raises if it is missing: there is no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"libsmla.so not built at {path}; run "
+                "python -m sparse_mla_attention_02_gb300.build")
+        lib = ctypes.CDLL(path)
+        P, I, I64, F, SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                            ctypes.c_float, ctypes.c_size_t)
+        fwd_args = [P, P, I, P, P, P, I, I, I, I, I, I64, F, P, P]
+        lib.smla_fwd.argtypes = fwd_args + [P]
+        lib.smla_fwd.restype = I
+        lib.smla_fwd_ws.argtypes = fwd_args + [P, SZ, P]
+        lib.smla_fwd_ws.restype = I
+        lib.smla_workspace_size.argtypes = [I, I, I, I, I, I]
+        lib.smla_workspace_size.restype = SZ
+        lib.smla_combine.argtypes = [P, P, I, I64, I, P, P, P]
+        lib.smla_combine.restype = I
+        lib.smla_get_device_status.argtypes = [ctypes.POINTER(I), I]
+        lib.smla_get_device_status.restype = I
+        lib.smla_status_string.argtypes = [I]
+        lib.smla_status_string.restype = ctypes.c_char_p
+        lib.smla_version.argtypes = []
+        lib.smla_version.restype = I
+        _lib = lib
+        return lib
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(code, what):
+    if code != SMLA_OK:
+        raise SmlaError(code, what)
+
+
+def _fwd_args(q, kv_cache, kv_dtype, k_scale, indices, valid_len, sm_scale,
+              out, lse, num_slots):
+    import torch
+    assert q.is_cuda and q.dtype == torch.bfloat16 and q.is_contiguous()
+    T, h, d_qk = q.shape
+    assert kv_cache.is_cuda and kv_cache.is_contiguous()
+    if kv_dtype == SMLA_KV_BF16:
+        assert kv_cache.dtype == torch.bfloat16
+    else:
+        assert kv_cache.dtype == torch.uint8
+        assert k_scale is not None and k_scale.dtype == torch.float32
+        assert k_scale.is_cuda and k_scale.is_contiguous()
+    S = kv_cache.numel() // d_qk if num_slots is None else int(num_slots)
+    assert indices.is_cuda and indices.dtype == torch.int32
+    assert indices.is_contiguous() and indices.shape[0] == T
+    topk = indices.shape[1]
+    if valid_len is not None:
+        assert valid_len.is_cuda and valid_len.dtype == torch.int32
+        assert valid_len.is_contiguous() and valid_len.shape == (T,)
+    d_v = 512
+    if out is None:
+        out = torch.empty((T, h, d_v), dtype=torch.bfloat16, device=q.device)
+    assert out.dtype == torch.bfloat16 and out.is_contiguous()
+    assert out.shape == (T, h, d_v)
+    if lse is not None:
+        assert lse.dtype == torch.float32 and lse.is_contiguous()
+        assert lse.shape == (T, h)
+    args = [_p(q), _p(kv_cache), int(kv_dtype), _p(k_scale), _p(indices),
+            _p(valid_len), T, h, d_qk, d_v, topk, S, float(sm_scale),
+            _p(out), _p(lse)]
+    return args, out, lse
+
+
+def smla_fwd(q, kv_cache, kv_dtype, k_scale, indices, valid_len, sm_scale,
+             out=None, lse=None, want_lse=True, num_slots=None, stream=None):
+    """Sparse MLA forward through ``smla_fwd`` (library-owned workspace).
+
+    q bf16 [T,h,d_qk]; kv_cache bf16 or uint8 [S,d_qk]; k_scale f32 or None;
+    indices int32 [T,topk]; valid_len int32 [T] or None.
+    Returns (out bf16 [T,h,512], lse f32 [T,h] or None)."""
+    import torch
+    lib = load()
+    if lse is None and want_lse:
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    args, out, lse = _fwd_args(q, kv_cache, kv_dtype, k_scale, indices,
+                               valid_len, sm_scale, out, lse, num_slots)
+    _check(lib.smla_fwd(*args, _stream(stream)), "smla_fwd")
+    return out, lse
+
+
+def smla_workspace_size(T, h, d_qk, topk, kv_dtype, d_v=512) -> int:
+    return int(load().smla_workspace_size(T, h, d_qk, d_v, topk, kv_dtype))
+
+
+def smla_fwd_ws(q, kv_cache, kv_dtype, k_scale, indices, valid_len, sm_scale,
+                workspace, out=None, lse=None, want_lse=True, num_slots=None,
+                stream=None):
+    """``smla_fwd_ws``: as smla_fwd with a caller-owned workspace tensor
+    (uint8 on the device, at least smla_workspace_size bytes)."""
+    import torch
+    lib = load()
+    if lse is None and want_lse:
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    args, out, lse = _fwd_args(q, kv_cache, kv_dtype, k_scale, indices,
+                               valid_len, sm_scale, out, lse, num_slots)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.smla_fwd_ws(*args, _p(workspace), nbytes, _stream(stream)),
+           "smla_fwd_ws")
+    return out, lse
+
+
+def smla_combine(o_parts, lse_parts, out=None, lse=None, stream=None):
+    """``smla_combine``: o_parts f32 [P, rows, 512], lse_parts f32 [P, rows]."""
+    import torch
+    lib = load()
+    P, rows, d_v = o_parts.shape
+    assert o_parts.dtype == torch.float32 and o_parts.is_contiguous()
+    assert lse_parts.dtype == torch.float32 and lse_parts.is_contiguous()
+    assert lse_parts.shape == (P, rows)
+    if out is None:
+        out = torch.empty((rows, d_v), dtype=torch.bfloat16, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty((rows,), dtype=torch.float32, device=o_parts.device)
+    _check(lib.smla_combine(_p(o_parts), _p(lse_parts), P, rows, d_v, _p(out),
+                            _p(lse), _stream(stream)), "smla_combine")
+    return out, lse
+
+
+def smla_get_device_status(clear=True) -> int:
+    v = ctypes.c_int(0)
+    _check(load().smla_get_device_status(ctypes.byref(v), int(clear)),
+           "smla_get_device_status")
+    return v.value
+
+
+def smla_status_string(code: int) -> str:
+    return load().smla_status_string(int(code)).decode()

@@ -1,0 +1,268 @@
+// smla_api.cu — the C ABI of libsmla: argument checks, the split plan,
+// workspace handling, the device status word, and kernel launches.
+//
+// Boundary as stated by the pages: FlashMLA's sparse forward takes
+// (q, kv, indices, sm_scale, d_v, topk_length) and returns (out, lse)
+// (vLLM API docs flashmla_sparse, FlashMLASparseImpl._bf16_flash_mla_kernel);
+// FlashInfer's run takes (q_nope, q_pe, ckv, kpe, ckv_scale, kpe_scale)
+// (flashinfer_mla_sparse_sm90.py, forward_mqa).  smla_fwd takes the
+// concatenated q, the cache, its scales, the slot ids and valid counts.
+#include <mutex>
+#include <vector>
+
+#include "../../include/smla.h"
+#include "smla_internal.h"
+
+namespace {
+
+__device__ int g_smla_status = 0;  // device status word (first error wins)
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int num_sms = 0;
+  int* status = nullptr;      // device address of g_smla_status
+  void* workspace = nullptr;  // library-owned workspace for smla_fwd
+  size_t workspace_bytes = 0;
+};
+
+std::mutex g_mutex;
+DeviceInfo g_dev[kMaxDevices];
+
+// Per-device facts, looked up once with that device current.
+smla_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return SMLA_ERR_CUDA;
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+        cudaSuccess)
+      return SMLA_ERR_CUDA;
+    void* st = nullptr;
+    if (cudaGetSymbolAddress(&st, g_smla_status) != cudaSuccess)
+      return SMLA_ERR_CUDA;
+    d.num_sms = sms;
+    d.status = static_cast<int*>(st);
+    d.ready = true;
+  }
+  *out = &d;
+  return SMLA_OK;
+}
+
+bool aligned(const void* p, size_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+smla_status check_args(const void* q, const void* kv, int kv_dtype,
+                       const float* k_scale, const int32_t* indices, int T,
+                       int h, int d_qk, int d_v, int topk, int64_t num_slots,
+                       const void* out) {
+  if (T < 0 || h < 1 || topk < 1 || num_slots < 1) return SMLA_ERR_INVALID_ARG;
+  if (h > 128) return SMLA_ERR_UNSUPPORTED;
+  if (d_qk != 512 && d_qk != 576) return SMLA_ERR_UNSUPPORTED;
+  if (d_v != 512) return SMLA_ERR_UNSUPPORTED;
+  if (num_slots > 0x7FFFFFFFLL) return SMLA_ERR_UNSUPPORTED;
+  if (kv_dtype < SMLA_KV_BF16 || kv_dtype > SMLA_KV_FP8_E4M3_GROUP128)
+    return SMLA_ERR_UNSUPPORTED;
+  if (T == 0) return SMLA_OK;
+  if (!q || !kv || !indices || !out) return SMLA_ERR_INVALID_ARG;
+  if (kv_dtype != SMLA_KV_BF16 && !k_scale) return SMLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16) ||
+      !aligned(indices, 4) || (k_scale && !aligned(k_scale, 4)))
+    return SMLA_ERR_INVALID_ARG;
+  return SMLA_OK;
+}
+
+smla_status run_fwd(const void* q, const void* kv, int kv_dtype,
+                    const float* k_scale, const int32_t* indices,
+                    const int32_t* valid_len, int T, int h, int d_qk, int d_v,
+                    int topk, int64_t num_slots, float sm_scale, void* out,
+                    float* lse, void* ws, size_t ws_bytes, bool own_ws,
+                    cudaStream_t stream) {
+  smla_status st = check_args(q, kv, kv_dtype, k_scale, indices, T, h, d_qk,
+                              d_v, topk, num_slots, out);
+  if (st != SMLA_OK || T == 0) return st;
+  if ((valid_len && !aligned(valid_len, 4)) || (lse && !aligned(lse, 4)))
+    return SMLA_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    if ((st = device_info(&dev)) != SMLA_OK) return st;
+  }
+  const smla::Plan plan =
+      smla::make_plan(T, h, d_qk, d_v, topk, kv_dtype, dev->num_sms);
+  if (plan.workspace_bytes > 0) {
+    if (own_ws) {
+      std::lock_guard<std::mutex> lk(g_mutex);
+      if (dev->workspace_bytes < plan.workspace_bytes) {
+        if (dev->workspace) cudaFree(dev->workspace);
+        dev->workspace = nullptr;
+        dev->workspace_bytes = 0;
+        if (cudaMalloc(&dev->workspace, plan.workspace_bytes) != cudaSuccess)
+          return SMLA_ERR_CUDA;
+        dev->workspace_bytes = plan.workspace_bytes;
+      }
+      ws = dev->workspace;
+    } else {
+      if (!ws || ws_bytes < plan.workspace_bytes) return SMLA_ERR_WORKSPACE;
+      if (!aligned(ws, 256)) return SMLA_ERR_INVALID_ARG;
+    }
+  }
+  smla::FwdParams p{};
+  p.q = q;
+  p.kv = kv;
+  p.k_scale = k_scale;
+  p.indices = indices;
+  p.valid_len = valid_len;
+  p.out = out;
+  p.lse = lse;
+  p.status = dev->status;
+  p.num_slots = num_slots;
+  p.kv_format = kv_dtype;
+  p.T = T;
+  p.h = h;
+  p.d_qk = d_qk;
+  p.d_v = d_v;
+  p.topk = topk;
+  p.splits = plan.splits;
+  p.split_len = plan.split_len;
+  p.sm_scale = sm_scale;
+  if (plan.splits > 1) {
+    p.o_part = static_cast<float*>(ws);
+    p.lse_part = p.o_part + (size_t)plan.splits * T * h * d_v;
+  }
+  if (smla::launch_simt(p, stream) != cudaSuccess) return SMLA_ERR_CUDA;
+  if (plan.splits > 1) {
+    if (smla::launch_combine(p.o_part, p.lse_part, plan.splits, (int64_t)T * h,
+                             d_v, out, lse, stream) != cudaSuccess)
+      return SMLA_ERR_CUDA;
+  }
+  return SMLA_OK;
+}
+
+}  // namespace
+
+namespace smla {
+
+// Split plan: enough (token, head group, range) units to fill every SM at
+// least twice; ranges are multiples of 32 positions.  The valid counts are
+// device data, so ranges are cut over topk, and a range past a token's valid
+// count yields an empty partial (0, -inf) that the combine ignores.
+Plan make_plan(int T, int h, int d_qk, int d_v, int topk, int kv_format,
+               int num_sms) {
+  (void)d_qk;
+  (void)kv_format;
+  Plan pl{};
+  pl.kind = kKernelSimt;
+  const int64_t groups = (h + 15) / 16;
+  const int64_t units = (int64_t)T * groups;
+  const int64_t want = 2LL * (num_sms > 0 ? num_sms : 1);
+  int splits = 1;
+  if (units < want) {
+    splits = (int)((want + units - 1) / units);
+    const int max_by_topk = (topk + 127) / 128;  // at least 128 positions each
+    if (splits > max_by_topk) splits = max_by_topk;
+    if (splits > 64) splits = 64;
+    if (splits < 1) splits = 1;
+  }
+  int len = (topk + splits - 1) / splits;
+  len = (len + 31) / 32 * 32;
+  splits = (topk + len - 1) / len;
+  pl.splits = splits;
+  pl.split_len = len;
+  pl.workspace_bytes =
+      splits > 1 ? sizeof(float) * (size_t)splits * T * h * (d_v + 1) : 0;
+  return pl;
+}
+
+}  // namespace smla
+
+extern "C" {
+
+smla_status smla_fwd(const void* q, const void* kv_cache, int kv_dtype,
+                     const float* k_scale, const int32_t* indices,
+                     const int32_t* valid_len, int T, int h, int d_qk, int d_v,
+                     int topk, int64_t num_slots, float sm_scale, void* out,
+                     float* lse, cudaStream_t stream) {
+  return run_fwd(q, kv_cache, kv_dtype, k_scale, indices, valid_len, T, h,
+                 d_qk, d_v, topk, num_slots, sm_scale, out, lse, nullptr, 0,
+                 true, stream);
+}
+
+smla_status smla_fwd_ws(const void* q, const void* kv_cache, int kv_dtype,
+                        const float* k_scale, const int32_t* indices,
+                        const int32_t* valid_len, int T, int h, int d_qk,
+                        int d_v, int topk, int64_t num_slots, float sm_scale,
+                        void* out, float* lse, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
+  return run_fwd(q, kv_cache, kv_dtype, k_scale, indices, valid_len, T, h,
+                 d_qk, d_v, topk, num_slots, sm_scale, out, lse, workspace,
+                 workspace_bytes, false, stream);
+}
+
+size_t smla_workspace_size(int T, int h, int d_qk, int d_v, int topk,
+                           int kv_dtype) {
+  if (T <= 0 || h < 1 || topk < 1) return 0;
+  DeviceInfo* dev = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    if (device_info(&dev) != SMLA_OK) return 0;
+  }
+  return smla::make_plan(T, h, d_qk, d_v, topk, kv_dtype, dev->num_sms)
+      .workspace_bytes;
+}
+
+smla_status smla_combine(const float* o_parts, const float* lse_parts,
+                         int n_parts, int64_t rows, int d_v, void* out,
+                         float* lse, cudaStream_t stream) {
+  if (n_parts < 1 || n_parts > 64 || rows < 0) return SMLA_ERR_INVALID_ARG;
+  if (d_v != 512) return SMLA_ERR_UNSUPPORTED;
+  if (rows == 0) return SMLA_OK;
+  if (!o_parts || !lse_parts || !out) return SMLA_ERR_INVALID_ARG;
+  if (!aligned(o_parts, 16) || !aligned(lse_parts, 4) || !aligned(out, 8) ||
+      (lse && !aligned(lse, 4)))
+    return SMLA_ERR_INVALID_ARG;
+  if (smla::launch_combine(o_parts, lse_parts, n_parts, rows, d_v, out, lse,
+                           stream) != cudaSuccess)
+    return SMLA_ERR_CUDA;
+  return SMLA_OK;
+}
+
+smla_status smla_get_device_status(int* status_out, int clear) {
+  if (!status_out) return SMLA_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    smla_status st = device_info(&dev);
+    if (st != SMLA_OK) return st;
+  }
+  if (cudaDeviceSynchronize() != cudaSuccess) return SMLA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, dev->status, sizeof v, cudaMemcpyDeviceToHost) !=
+      cudaSuccess)
+    return SMLA_ERR_CUDA;
+  if (clear && cudaMemset(dev->status, 0, sizeof v) != cudaSuccess)
+    return SMLA_ERR_CUDA;
+  *status_out = v;
+  return SMLA_OK;
+}
+
+const char* smla_status_string(int status) {
+  switch (status) {
+    case SMLA_OK: return "SMLA_OK";
+    case SMLA_ERR_INVALID_ARG: return "SMLA_ERR_INVALID_ARG";
+    case SMLA_ERR_UNSUPPORTED: return "SMLA_ERR_UNSUPPORTED";
+    case SMLA_ERR_CUDA: return "SMLA_ERR_CUDA";
+    case SMLA_ERR_TIMEOUT: return "SMLA_ERR_TIMEOUT";
+    case SMLA_ERR_BAD_INDEX: return "SMLA_ERR_BAD_INDEX";
+    case SMLA_ERR_WORKSPACE: return "SMLA_ERR_WORKSPACE";
+    default: return "SMLA_ERR_UNKNOWN";
+  }
+}
+
+int smla_version(void) { return 100; }
+
+}  // extern "C"

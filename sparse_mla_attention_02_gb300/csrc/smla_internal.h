@@ -1,0 +1,55 @@
+// smla_internal.h — declarations shared by the CUDA translation units of
+// libsmla (host API, kernels).  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace smla {
+
+enum KvFormat { kBf16 = 0, kE4m3 = 1, kE4m3Group = 2 };
+
+// Bits of the device status word (first condition wins, see smla_api.cu).
+enum StatusBits { kStatusTimeout = 4, kStatusBadIndex = 5 };
+
+// Everything a forward launch needs.  Pointers are device pointers.
+struct FwdParams {
+  const void* q;          // bf16 [T, h, d_qk]
+  const void* kv;         // [num_slots, d_qk] bf16 or E4M3 bytes
+  const float* k_scale;   // per-tensor [1] or group [num_slots, G]
+  const int32_t* indices; // [T, topk]
+  const int32_t* valid_len;  // [T] or nullptr
+  void* out;              // bf16 [T, h, d_v]
+  float* lse;             // [T, h] or nullptr
+  float* o_part;          // split partials [splits, T, h, d_v] (splits > 1)
+  float* lse_part;        // [splits, T, h]
+  int* status;            // device status word
+  int64_t num_slots;
+  int kv_format;
+  int T, h, d_qk, d_v, topk;
+  int splits;             // top-k position ranges per (token, head group)
+  int split_len;          // positions per range
+  float sm_scale;
+};
+
+// Which kernel family a plan uses.
+enum KernelKind { kKernelSimt = 0, kKernelTc = 1 };
+
+struct Plan {
+  int kind;
+  int splits;
+  int split_len;
+  size_t workspace_bytes;   // partial O and LSE for splits > 1, else 0
+};
+
+Plan make_plan(int T, int h, int d_qk, int d_v, int topk, int kv_format,
+               int num_sms);
+
+cudaError_t launch_simt(const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_combine(const float* o_parts, const float* lse_parts,
+                           int n_parts, int64_t rows, int d_v, void* out,
+                           float* lse, cudaStream_t stream);
+
+}  // namespace smla

@@ -276,3 +276,24 @@ def custom(T, h, d_qk=576, d_v=512, topk=64, num_slots=256, kv_dtype=KV_BF16,
                     (1.0 / math.sqrt(d_qk)) if sm_scale is None else sm_scale,
                     q, kv, scales, torch.from_numpy(idx).to(device),
                     torch.from_numpy(valid).to(device), h)
+
+
+def token_subset(w: Workload, sel, device="cpu") -> Workload:
+    """Tokens `sel` of `w`, with a compact copy of only the cache rows (and
+    group scales) they select, ids remapped into it; -1 and out-of-range ids
+    stay masked.  Lets a checker see a few tokens of a multi-GB pool."""
+    sel_t = torch.as_tensor(np.asarray(sel, dtype=np.int64),
+                            device=w.indices.device)
+    idx = w.indices[sel_t].long()
+    ok = (idx >= 0) & (idx < w.num_slots)
+    rows = torch.unique(idx[ok])
+    remap = torch.searchsorted(rows, idx.clamp(min=0))
+    new_idx = torch.where(ok, remap, torch.full_like(remap, -1)).int()
+    ks = w.k_scale
+    if ks is not None and ks.dim() == 2:
+        ks = ks[rows]
+    mv = lambda x: None if x is None else x.to(device)
+    return Workload(w.name, int(sel_t.numel()), w.h, w.d_qk, w.d_v, w.topk,
+                    max(1, int(rows.numel())), w.kv_dtype, w.sm_scale,
+                    mv(w.q[sel_t]), mv(w.kv[rows]), mv(ks), mv(new_idx),
+                    mv(w.valid_len[sel_t]), w.real_heads, dict(w.notes))

@@ -1,0 +1,90 @@
+"""The C ABI without a GPU: the library loads, exports every entry point the
+header declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_mla_attention_02_gb300 as smla
+from sparse_mla_attention_02_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "smla.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return smla.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"SMLA_API\s+[\w\s\*]+?\b(smla_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for n in ["smla_fwd", "smla_fwd_ws", "smla_workspace_size", "smla_combine",
+              "smla_get_device_status", "smla_status_string", "smla_version"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_symbols():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code, name in smla.STATUS_NAMES.items():
+        assert smla.smla_status_string(code) == name
+    assert smla.smla_status_string(99) == "SMLA_ERR_UNKNOWN"
+    assert lib.smla_version() >= 100
+
+
+def _fwd(lib, **kw):
+    a = dict(q=1 << 12, kv=1 << 12, kv_dtype=0, k_scale=None, idx=1 << 12,
+             valid=None, T=4, h=16, d_qk=576, d_v=512, topk=64, S=256,
+             scale=0.04, out=1 << 12, lse=None)
+    a.update(kw)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.smla_fwd(P(a["q"]), P(a["kv"]), a["kv_dtype"], P(a["k_scale"]),
+                        P(a["idx"]), P(a["valid"]), a["T"], a["h"], a["d_qk"],
+                        a["d_v"], a["topk"], a["S"], a["scale"], P(a["out"]),
+                        P(a["lse"]), None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=-1), 1), (dict(h=0), 1), (dict(topk=0), 1), (dict(S=0), 1),
+    (dict(h=129), 2), (dict(d_qk=128), 2), (dict(d_v=256), 2),
+    (dict(kv_dtype=3), 2), (dict(S=1 << 31), 2),
+    (dict(q=None), 1), (dict(kv=None), 1), (dict(idx=None), 1),
+    (dict(out=None), 1), (dict(kv_dtype=1), 1), (dict(kv_dtype=2), 1),
+    (dict(q=(1 << 12) + 8), 1), (dict(out=(1 << 12) + 4), 1),
+    (dict(idx=(1 << 12) + 2), 1),
+])
+def test_bad_arguments_are_rejected_on_the_host(lib, kw, code):
+    assert _fwd(lib, **kw) == code
+
+
+def test_zero_tokens_is_ok_and_launches_nothing(lib):
+    assert _fwd(lib, T=0, q=None, kv=None, idx=None, out=None) == 0
+
+
+def test_combine_argument_checks(lib):
+    P = ctypes.c_void_p
+    c = lib.smla_combine
+    assert c(P(4096), P(4096), 0, 10, 512, P(4096), None, None) == 1
+    assert c(P(4096), P(4096), 65, 10, 512, P(4096), None, None) == 1
+    assert c(P(4096), P(4096), 2, 10, 256, P(4096), None, None) == 2
+    assert c(None, P(4096), 2, 10, 512, P(4096), None, None) == 1
+    assert c(P(4100), P(4096), 2, 10, 512, P(4096), None, None) == 1
+    assert c(None, None, 2, 0, 512, None, None, None) == 0
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(smla, "_lib", None)
+    monkeypatch.setattr(build, "LIB", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        smla.load()
