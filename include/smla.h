@@ -144,6 +144,48 @@ SMLA_API smla_status smla_combine(const float* o_parts, const float* lse_parts,
                          int n_parts, int64_t rows, int d_v, void* out,
                          float* lse, cudaStream_t stream);
 
+/* Bytes of the fixed device scratch behind smla_fwd_noalloc (16 MiB). */
+#define SMLA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * smla_fwd_noalloc — the same forward as smla_fwd, for callers that cannot
+ * allocate device memory.  The pages have no counterpart to this entry
+ * point; it exists for how the library is hosted, not for the method.
+ *
+ * Who needs it: code that runs inside a host which owns every byte of device
+ * memory through its own pool (an inference engine's plugin, a framework
+ * that forbids cudaMalloc outside its allocator so its accounting stays
+ * exact), and latency-critical loops where a cudaMalloc, which may stall
+ * until the device is idle, is not acceptable.  Such a caller passes its
+ * inputs and outputs exactly as for smla_fwd and nothing else.
+ *
+ * Scratch: the split partial results go to a device array of
+ * SMLA_NOALLOC_SCRATCH_BYTES that is part of the library itself; every GPU
+ * on which the library is loaded holds it until the process exits.  This
+ * function calls no cudaMalloc, cudaFree or other allocating routine.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current) and keeps it; make that first call before any
+ *    stream capture.
+ *  - A shape whose split plan needs more than SMLA_NOALLOC_SCRATCH_BYTES
+ *    (smla_workspace_size tells in advance) returns SMLA_ERR_WORKSPACE and
+ *    launches nothing.
+ *  - All calls share the one array, and it keeps whatever the last call
+ *    left.  Nothing in it has to start at zero: each call writes every
+ *    partial it later reads.  But two calls that may run at the same time on
+ *    the GPU (different streams, or different host threads) race on the array
+ *    and corrupt each other's results: keep such calls on one stream, or use
+ *    smla_fwd_ws with one workspace per stream.
+ * Arguments, layouts and the other error codes are those of smla_fwd.
+ */
+SMLA_API smla_status smla_fwd_noalloc(const void* q, const void* kv_cache,
+                                      int kv_dtype, const float* k_scale,
+                                      const int32_t* indices,
+                                      const int32_t* valid_len, int T, int h,
+                                      int d_qk, int d_v, int topk,
+                                      int64_t num_slots, float sm_scale,
+                                      void* out, float* lse,
+                                      cudaStream_t stream);
+
 /*
  * smla_get_device_status — read (and optionally clear) the current device's
  * status word: 0, or the SMLA_ERR_TIMEOUT / SMLA_ERR_BAD_INDEX condition
