@@ -134,7 +134,10 @@ smla_status run_fwd(const void* q, const void* kv, int kv_dtype,
     p.o_part = static_cast<float*>(ws);
     p.lse_part = p.o_part + (size_t)plan.splits * T * h * d_v;
   }
-  if (smla::launch_simt(p, stream) != cudaSuccess) return SMLA_ERR_CUDA;
+  const cudaError_t le = plan.kind == smla::kKernelTc
+                            ? smla::launch_tc(p, stream)
+                            : smla::launch_simt(p, stream);
+  if (le != cudaSuccess) return SMLA_ERR_CUDA;
   if (plan.splits > 1) {
     if (smla::launch_combine(p.o_part, p.lse_part, plan.splits, (int64_t)T * h,
                              d_v, out, lse, stream) != cudaSuccess)
@@ -147,29 +150,44 @@ smla_status run_fwd(const void* q, const void* kv, int kv_dtype,
 
 namespace smla {
 
-// Split plan: enough (token, head group, range) units to fill every SM at
-// least twice; ranges are multiples of 32 positions.  The valid counts are
-// device data, so ranges are cut over topk, and a range past a token's valid
-// count yields an empty partial (0, -inf) that the combine ignores.
+// Split plan.  Valid counts are device data, so ranges are cut over topk; a
+// range past a token's valid count yields an empty partial (0, -inf) that the
+// combine ignores.
+//  - tensor-core path: one unit = (token, range) on a 2-SM cluster, one
+//    cluster per two SMs resident; split only when the tokens alone leave
+//    more than half of the pairs idle (each split costs partial-O traffic).
+//  - CUDA-core path: enough (token, 16-head group, range) units to fill every
+//    SM twice.
 Plan make_plan(int T, int h, int d_qk, int d_v, int topk, int kv_format,
                int num_sms) {
-  (void)d_qk;
-  (void)kv_format;
   Plan pl{};
-  pl.kind = kKernelSimt;
-  const int64_t groups = (h + 15) / 16;
-  const int64_t units = (int64_t)T * groups;
-  const int64_t want = 2LL * (num_sms > 0 ? num_sms : 1);
-  int splits = 1;
-  if (units < want) {
-    splits = (int)((want + units - 1) / units);
-    const int max_by_topk = (topk + 127) / 128;  // at least 128 positions each
-    if (splits > max_by_topk) splits = max_by_topk;
-    if (splits > 64) splits = 64;
-    if (splits < 1) splits = 1;
+  int splits = 1, gran = 32;
+  if (tc_supported(h, d_qk, kv_format)) {
+    pl.kind = kKernelTc;
+    gran = 64;
+    const int pairs = num_sms > 1 ? num_sms / 2 : 1;
+    if (2LL * T < pairs) {
+      splits = pairs / (T > 0 ? T : 1);
+      const int max_by_topk = (topk + 127) / 128;
+      if (splits > max_by_topk) splits = max_by_topk;
+      if (splits > 16) splits = 16;
+      if (splits < 1) splits = 1;
+    }
+  } else {
+    pl.kind = kKernelSimt;
+    const int64_t groups = (h + 15) / 16;
+    const int64_t units = (int64_t)T * groups;
+    const int64_t want = 2LL * (num_sms > 0 ? num_sms : 1);
+    if (units < want) {
+      splits = (int)((want + units - 1) / units);
+      const int max_by_topk = (topk + 127) / 128;
+      if (splits > max_by_topk) splits = max_by_topk;
+      if (splits > 64) splits = 64;
+      if (splits < 1) splits = 1;
+    }
   }
   int len = (topk + splits - 1) / splits;
-  len = (len + 31) / 32 * 32;
+  len = (len + gran - 1) / gran * gran;
   splits = (topk + len - 1) / len;
   pl.splits = splits;
   pl.split_len = len;

@@ -68,20 +68,32 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
-// Bounded wait: returns false if the phase did not complete within the
-// iteration budget (the caller records a timeout instead of hanging).
-constexpr uint32_t kSpinLimit = 1u << 24;
-
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
 }
 
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-  return false;
+// Bounded wait: returns false if the phase did not complete within
+// kWaitLimitNs, or as soon as *stop equals stop_value (another block gave
+// up), so that the caller records a timeout instead of hanging.
+constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;
+
+template <bool kCluster>
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  const volatile int* stop,
+                                                  int stop_value) {
+  if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))
+    return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))
+      return true;
+    if ((i & 255u) == 0u) {
+      if (*stop == stop_value) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+  }
 }
 
 // -------------------------------------------------------------- cp.async --
