@@ -187,9 +187,12 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.Stream(dev)
     pk, pk_src = peaks()
 
-    def setup(name, seed_shift):
+    def setup(name, seed_shift, tokens=0):
         w = W.CONFIGS[name](device=dev, seed=1000 + list(W.CONFIGS).index(name)
                             + 7919 * seed_shift)
+        if tokens and tokens < w.T:
+            # the last `tokens` tokens (same kernel, a smaller launch)
+            w = W.token_subset(w, np.arange(w.T - tokens, w.T), device=dev)
         n = smla.smla_workspace_size(w.T, w.h, w.d_qk, w.topk, w.kv_dtype)
         ws = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
         out = torch.empty((w.T, w.h, w.d_v), dtype=torch.bfloat16, device=dev)
@@ -215,7 +218,7 @@ def run_ours(args, rank, world, local_rank):
         return float(t.item())
 
     # ---- headline: bf16 prefill --------------------------------------------
-    w, ws, out, lse, ws_n = setup(args.config, rank)
+    w, ws, out, lse, ws_n = setup(args.config, rank, args.tokens)
     fl = flops_of(w)
     U, G = bytes_model(w)
     f = step_fn(w, ws, out, lse)
@@ -252,6 +255,14 @@ def run_ours(args, rank, world, local_rank):
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     roof["frac_of_sustained"] = round(achieved / pk["bf16_tflops_sustained"], 4) \
         if bound_tensor else None
+
+    if args.main_only:
+        if rank == 0:
+            print(json.dumps({"config": args.config, "T": w.T,
+                              "ms_per_step": round(ms, 4),
+                              "tflops": round(value, 3),
+                              "flops_per_launch": fl, "U": U, "G": G}), flush=True)
+        return
 
     # ---- e2e: host buffers, copies inside the timed region -----------------
     h_q = torch.empty(w.q.shape, dtype=w.q.dtype, pin_memory=True)
@@ -457,6 +468,10 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=32)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="use only the last N tokens of the config (profiling)")
+    ap.add_argument("--main-only", action="store_true",
+                    help="time only the main step loop (profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

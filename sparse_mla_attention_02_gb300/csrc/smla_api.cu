@@ -173,6 +173,8 @@ Plan make_plan(int T, int h, int d_qk, int d_v, int topk, int kv_format,
       if (splits > 16) splits = 16;
       if (splits < 1) splits = 1;
     }
+    const int need = (topk + tc_max_range() - 1) / tc_max_range();
+    if (splits < need) splits = need;
   } else {
     pl.kind = kKernelSimt;
     const int64_t groups = (h + 15) / 16;

@@ -49,6 +49,7 @@ Plan make_plan(int T, int h, int d_qk, int d_v, int topk, int kv_format,
 
 cudaError_t launch_simt(const FwdParams& p, cudaStream_t stream);
 bool tc_supported(int h, int d_qk, int kv_format);
+int tc_max_range();  // largest top-k range one tensor-core unit covers
 cudaError_t launch_tc(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_combine(const float* o_parts, const float* lse_parts,
                            int n_parts, int64_t rows, int d_v, void* out,

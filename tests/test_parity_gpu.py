@@ -120,6 +120,22 @@ def test_mixed_prefill_decode_batch(cuda_lib):
     check(cuda_lib, w)
 
 
+@pytest.mark.parametrize("valid", [48, 96, 144, None])
+def test_many_waves_short_ranges(cuda_lib, valid):
+    """Several waves of clusters, each unit only 1-3 blocks long, repeated:
+    the end-of-unit hand-offs (last PV, epilogue) run while the previous PVs
+    may still be in flight."""
+    T = 200
+    vl = [valid] * T if valid is not None else None
+    w = W.custom(T=T, h=128, topk=valid or 128, num_slots=2048, valid=vl,
+                 seed=60 + (valid or 0), name=f"waves_v{valid}")
+    wd = w.to("cuda")
+    Or, Lr = oracle_fwd(w)
+    for _ in range(3):
+        O, L = gpu_fwd(cuda_lib, wd)
+        compare(O, L, Or, Lr, w.name)
+
+
 @pytest.mark.parametrize("kv_dtype", [0, 1, 2])
 def test_scattered_minus_one_and_out_of_range(cuda_lib, kv_dtype):
     w = W.custom(T=3, h=64, topk=96, num_slots=500, kv_dtype=kv_dtype,
