@@ -25,7 +25,8 @@
 // rows give (O = 0, LSE = -inf)):
 //   a1 work setup: v = min(valid_len[t], topk); range [k0, k1) of the split
 //   a2 gather: slot ids -> rows of the cache into a 128-byte-swizzled tile
-//      (masked positions become zero rows and -inf scores)
+//      with TMA tile::gather4 (masked positions read the out-of-bounds
+//      zero fill and get -inf scores)
 //   a4 QK^T (tcgen05.mma, A = Q from TMEM, B = K tile, K-major)
 //   a5 masked online softmax in registers (one thread per head row), running
 //      max updated lazily (O is rescaled only when the max grows by > 2^8)
@@ -33,14 +34,18 @@
 //   a7 epilogue: O / l -> bf16 out (or fp32 partials), LSE = m + ln l
 //
 // Warp roles (288 threads): warp 0 issues MMAs (warp-uniform code, one
-// elected lane per batch of MMAs) and owns TMEM; warps 1..3 gather with
-// cp.async; warps 4..7 (a warpgroup; thread i <-> TMEM lane i <-> head i) run
+// elected lane per batch of MMAs) and owns TMEM; warps 1..3 load the unit's
+// slot ids, then gather with TMA; warps 4..7 (a warpgroup; thread i <-> TMEM lane i <-> head i) run
 // softmax, the exchange, O rescale and the epilogue; warp 8 signals the peer
 // when its partial scores have been consumed.
 // Every wait is bounded; a wait that runs out records a timeout status, sets
 // an abort flag that skips later waits, and the block finishes normally.
+#include <cuda.h>
 #include <cuda_bf16.h>
+#include <cudaTypedefs.h>
 #include <math.h>
+
+#include <mutex>
 
 #include "smla_internal.h"
 #include "tc_ptx.cuh"
@@ -59,7 +64,7 @@ constexpr int kXStride = 52;               // floats per exchanged S row (padded
 constexpr int kXBytes = 128 * kXStride * 4;
 constexpr uint32_t kXTxBytes = 128u * kBN * 4u;  // bytes received per block
 constexpr int kThreads = 288;            // 8 role warps + 1 signal warp
-constexpr int kProducers = 96;             // warps 1..3
+constexpr int kProducers = 96;             // warps 1..3 (slot-id prefetch)
 
 // TMEM columns.
 constexpr uint32_t kColO = 0;              // O half: 256 columns
@@ -96,11 +101,13 @@ constexpr uint32_t kSmemBytes = kOffAbort + 4 + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kColS + 2 * kBN <= kTmemCols, "TMEM budget");
 static_assert(kAtomBytes % 1024 == 0, "swizzle atoms must stay 1024-aligned");
+static_assert(kBN % 12 == 0, "three producer warps split the 4-row groups evenly");
 
 struct TcArgs {
+  CUtensorMap kv_map;  // the cache as a 2-D tensor [num_slots, d_qk], 64-channel boxes
   FwdParams p;
   int g_lo[2];      // first cache channel gathered by CTA r
-  int n_chunks[2];  // 16-byte chunks gathered per row by CTA r
+  int n_boxes[2];   // 64-channel boxes gathered per row by CTA r
   int qk_lo[2];     // first local channel of CTA r's QK range
   int q_lo[2];      // first q channel CTA r keeps in TMEM
   int ksteps;       // 16-channel MMA steps of the QK half
@@ -168,7 +175,7 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(kBarKvFull + s), 2 * kProducers);
+      mbar_init(bar(kBarKvFull + s), 3);      // one expect_tx per producer warp
       mbar_init(bar(kBarKvEmpty + s), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -288,33 +295,34 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
       }
     }
   } else if (warp < 4) {
-    // ---- producers: a2 gather ---------------------------------------------
-    const int pt = tid - 32;
-    const int nc = a.n_chunks[r];
+    // ---- producers: a2 gather with TMA (tile::gather4) ----------------------
+    // Per block: 12 groups of 4 rows x n_boxes 64-channel boxes; warps 1..3
+    // each issue 4 of the groups (TMA gather throughput grows with the number
+    // of issuing warps).  The tensor map's 128-byte swizzle matches the MMA
+    // operand layout, and a masked position (slot id -1) reads the
+    // out-of-bounds fill, i.e. a zero row.
     const int g_lo = a.g_lo[r];
-    const size_t row_bytes = (size_t)p.d_qk * 2;
-    const uint8_t* kv = reinterpret_cast<const uint8_t*>(p.kv);
-    // Two threads per row (96 = 2 x 48); thread half h copies the 16-byte
-    // chunks h, h+2, h+4, ... of its row, so neighbouring lanes read
-    // neighbouring 16-byte pieces of one row.
-    const int row = pt >> 1, half = pt & 1;
-    const uint32_t sw = (uint32_t)row & 7u;
+    const int n_boxes = a.n_boxes[r];
+    const int w = warp - 1;                                   // 0..2
+    const uint32_t tx_bytes = (uint32_t)(kBN / 4 / 3 * n_boxes * 512);
     for (int b = 0; b < nb; ++b) {
       const int s = b % kStages;
       if (b >= kStages) W.wait(bar(kBarKvEmpty + s), ((b / kStages) - 1) & 1);
-      const uint32_t rdst = sb + kOffTile + s * kTileBytes + row * 128;
-      const int id = slots[b * kBN + row];
-      const uint8_t* src = kv + (size_t)(id < 0 ? 0 : id) * row_bytes + (size_t)g_lo * 2;
-      const uint32_t nbytes = id < 0 ? 0u : 16u;
-      for (int cj = half; cj < nc; cj += 2) {
-        const uint32_t dst =
-            rdst + (cj >> 3) * kAtomBytes + ((((uint32_t)cj & 7u) ^ sw) << 4);
-        cp_async_16(dst, src + 16 * cj, nbytes);
+      __syncwarp();
+      if (elect_one()) {
+        const uint32_t full = bar(kBarKvFull + s);
+        mbar_arrive_expect_tx(full, tx_bytes);
+        const uint32_t tile = sb + kOffTile + s * kTileBytes;
+        const int* bs = slots + b * kBN;
+        for (int g = w; g < kBN / 4; g += 3) {
+          const int y0 = bs[4 * g], y1 = bs[4 * g + 1], y2 = bs[4 * g + 2], y3 = bs[4 * g + 3];
+          for (int bx = 0; bx < n_boxes; ++bx)
+            tma_gather4(tile + bx * kAtomBytes + 4 * g * 128, &a.kv_map, g_lo + 64 * bx, y0,
+                        y1, y2, y3, full);
+        }
       }
-      cp_async_mbar_arrive(bar(kBarKvFull + s));
-      mbar_arrive(bar(kBarKvFull + s));
+      __syncwarp();
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == 8) {
     // ---- signal warp: tell the peer when its partial scores were consumed --
     // (a release-ordered remote arrival; kept off the softmax warps' path)
@@ -552,16 +560,43 @@ bool tc_supported(int h, int d_qk, int kv_format) {
   return h >= 1 && h <= 128 && (d_qk == 576 || d_qk == 512) && kv_format == kBf16;
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (the library does not link libcuda directly).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
 cudaError_t launch_tc(const FwdParams& p, cudaStream_t stream) {
   TcArgs a{};
   a.p = p;
+  auto encode = tensor_map_encoder();
+  if (!encode) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)p.d_qk, (cuuint64_t)p.num_slots};
+  const cuuint64_t strides[1] = {(cuuint64_t)p.d_qk * 2};
+  const cuuint32_t box[2] = {64, 1};
+  const cuuint32_t estr[2] = {1, 1};
+  if (encode(&a.kv_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.kv), dims,
+             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
   if (p.d_qk == 576) {
-    a.g_lo[0] = 0;   a.n_chunks[0] = 36; a.qk_lo[0] = 0;  a.q_lo[0] = 0;
-    a.g_lo[1] = 256; a.n_chunks[1] = 40; a.qk_lo[1] = 32; a.q_lo[1] = 288;
+    a.g_lo[0] = 0;   a.n_boxes[0] = 5; a.qk_lo[0] = 0;  a.q_lo[0] = 0;
+    a.g_lo[1] = 256; a.n_boxes[1] = 5; a.qk_lo[1] = 32; a.q_lo[1] = 288;
     a.ksteps = 18;
   } else {
-    a.g_lo[0] = 0;   a.n_chunks[0] = 32; a.qk_lo[0] = 0; a.q_lo[0] = 0;
-    a.g_lo[1] = 256; a.n_chunks[1] = 32; a.qk_lo[1] = 0; a.q_lo[1] = 256;
+    a.g_lo[0] = 0;   a.n_boxes[0] = 4; a.qk_lo[0] = 0; a.q_lo[0] = 0;
+    a.g_lo[1] = 256; a.n_boxes[1] = 4; a.qk_lo[1] = 0; a.q_lo[1] = 256;
     a.ksteps = 16;
   }
   a.scale_log2 = p.sm_scale * 1.4426950408889634f;

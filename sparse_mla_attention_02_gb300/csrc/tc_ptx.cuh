@@ -139,6 +139,18 @@ __device__ __forceinline__ void st_cluster_b32(uint32_t addr, uint32_t a) {
   asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(addr), "r"(a) : "memory");
 }
 
+// TMA gather: four rows (y0..y3) of a 2-D tensor map, one box of columns
+// starting at x each, into four consecutive 128-byte rows at dst; the bytes
+// are counted on the mbarrier (complete_tx).  Out-of-range rows read zeros.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int x, int y0,
+                                            int y1, int y2, int y3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::"
+      "bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
+      : "memory");
+}
+
 // Asynchronous 16-byte store into another CTA's shared memory; its bytes are
 // counted on that CTA's mbarrier (complete_tx), which the receiver arms with
 // the expected byte count.
