@@ -60,9 +60,10 @@ constexpr int kStages = 4;                 // gathered-tile pipeline depth
 constexpr int kAtomBytes = kBN * 128;      // 48 rows x 128 B (64 channels)
 constexpr int kTileBytes = 5 * kAtomBytes; // up to 320 channels per CTA
 constexpr int kPBytes = 128 * 128;         // P: 128 rows x 64 bf16 (48 used)
-constexpr int kXStride = 52;               // floats per exchanged S row (padded)
-constexpr int kXBytes = 128 * kXStride * 4;
-constexpr uint32_t kXTxBytes = 128u * kBN * 4u;  // bytes received per block
+// Exchanged partial scores: 128 rows x 48 fp32; the 16-byte chunk c of row i
+// sits at chunk position c ^ (i & 3) (conflict-light row access, no padding).
+constexpr int kXBytes = 128 * kBN * 4;
+constexpr uint32_t kXTxBytes = (uint32_t)kXBytes;  // bytes received per block
 constexpr int kThreads = 288;            // 8 role warps + 1 signal warp
 constexpr int kProducers = 96;             // warps 1..3 (slot-id prefetch)
 
@@ -74,10 +75,11 @@ constexpr uint32_t kTmemCols = 512;
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
 constexpr uint32_t kOffTile = 0;
-constexpr uint32_t kOffP = kOffTile + kStages * kTileBytes;
-constexpr uint32_t kOffX = kOffP + 2 * kPBytes;
+constexpr uint32_t kOffP = kOffTile + kStages * kTileBytes;   // one P buffer
+constexpr uint32_t kOffX = kOffP + kPBytes;                    // receive [2]
+constexpr uint32_t kOffXs = kOffX + 2 * kXBytes;               // send staging
 constexpr int kMaxBlocks = 64;             // covers topk <= 3072 in one range
-constexpr uint32_t kOffSlot = kOffX + 2 * kXBytes;              // [blocks*48] i32
+constexpr uint32_t kOffSlot = kOffXs + kXBytes;                 // [blocks*48] i32
 constexpr uint32_t kOffMask = kOffSlot + kMaxBlocks * kBN * 4;  // [blocks][2] u32
 constexpr uint32_t kOffBar = (kOffMask + kMaxBlocks * 8 + 7) & ~7u;
 enum {
@@ -85,9 +87,9 @@ enum {
   kBarKvEmpty = kBarKvFull + kStages,
   kBarSFull = kBarKvEmpty + kStages,   // [2]
   kBarSEmpty = kBarSFull + 2,          // [2]
-  kBarPFull = kBarSEmpty + 2,          // [2]
-  kBarPEmpty = kBarPFull + 2,          // [2]
-  kBarXFull = kBarPEmpty + 2,          // [2]
+  kBarPFull = kBarSEmpty + 2,
+  kBarPEmpty,
+  kBarXFull,                           // [2]
   kBarXFree = kBarXFull + 2,           // [2]
   kBarXCons = kBarXFree + 2,           // [2]
   kBarODone = kBarXCons + 2,
@@ -181,12 +183,12 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarSFull + i), 1);
       mbar_init(bar(kBarSEmpty + i), 128);
-      mbar_init(bar(kBarPFull + i), 128);
-      mbar_init(bar(kBarPEmpty + i), 1);
       mbar_init(bar(kBarXFull + i), 1);
       mbar_init(bar(kBarXFree + i), 1);
       mbar_init(bar(kBarXCons + i), 128);
     }
+    mbar_init(bar(kBarPFull), 128);
+    mbar_init(bar(kBarPEmpty), 1);
     mbar_init(bar(kBarODone), 1);
     mbar_init(bar(kBarOFinal), 1);
     mbar_init(bar(kBarQReady), 128);
@@ -266,11 +268,10 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
         __syncwarp();
       };
       auto issue_pv = [&](int j) {
-        const int buf = j & 1;
-        W.wait(bar(kBarPFull + buf), (j >> 1) & 1);
+        W.wait(bar(kBarPFull), j & 1);
         __syncwarp();
         tc_fence_after();
-        const uint32_t pa = sb + kOffP + buf * kPBytes;
+        const uint32_t pa = sb + kOffP;
         const uint32_t tile = sb + kOffTile + (j % kStages) * kTileBytes;
         if (elect_one()) {
           fence_proxy_async_smem();
@@ -281,7 +282,7 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
             mma_ss(tmem + kColO, ad, bd, id_pv, (j > 0 || ks > 0) ? 1u : 0u);
           }
           mma_commit(bar(kBarODone));
-          mma_commit(bar(kBarPEmpty + buf));
+          mma_commit(bar(kBarPEmpty));
           mma_commit(bar(kBarKvEmpty + (j % kStages)));
           if (j == nb - 1) mma_commit(bar(kBarOFinal));
         }
@@ -369,8 +370,10 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
     float m_run = -INFINITY;   // running max (log2 units)
     float l_run = 0.f;         // running sum of exp2(s - m_run)
     const float* Xs = reinterpret_cast<const float*>(sm + kOffX);
-    const uint32_t x_peer_row = mapa(sb + kOffX, peer) + (uint32_t)i * kXStride * 4;
+    const uint32_t x_peer = mapa(sb + kOffX, peer);
     const uint32_t xfull_peer = mapa(bar(kBarXFull), peer);
+    const uint32_t xrow = (uint32_t)i * kBN * 4;      // this row's byte offset
+    const uint32_t xsw = (uint32_t)i & 3u;            // its chunk swizzle
 
     // O row *= alpha.  tcgen05.ld/st are warp-collective (.sync.aligned), so
     // the whole warp takes this path when any of its lanes needs it; lanes
@@ -391,10 +394,14 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
       tmem_wait_st();
     };
     // Read this row's partial scores of block j from TMEM, free the S buffer,
-    // and send them to the peer (X buffer j&1, counted on its X-full barrier).
+    // stage them in shared memory, and (thread 0) send all 128 rows to the
+    // peer with one bulk copy counted on its X-full barrier for buffer j&1.
     auto load_and_send = [&](int j, float (&dst)[kBN]) {
       const int buf = j & 1;
-      if (i == 0) mbar_arrive_expect_tx(bar(kBarXFull + buf), kXTxBytes);
+      if (i == 0) {
+        mbar_arrive_expect_tx(bar(kBarXFull + buf), kXTxBytes);
+        bulk_wait_read_all();                // the previous send has read the stage
+      }
       W.wait(bar(kBarSFull + buf), (j >> 1) & 1);
       __syncwarp();
       tc_fence_after();
@@ -408,13 +415,19 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
       }
       tc_fence_before();
       mbar_arrive(bar(kBarSEmpty + buf));
-      if (j >= 2) W.wait(bar(kBarXFree + buf), ((j >> 1) - 1) & 1);
-      const uint32_t xd = x_peer_row + buf * kXBytes;
-      const uint32_t xb = xfull_peer + 8u * buf;
+      named_bar_sync(2, 128);                // staging buffer is free
+      uint8_t* srow = sm + kOffXs + xrow;
 #pragma unroll
-      for (int c = 0; c < kBN; c += 4)
-        st_async_v4(xd + c * 4, __float_as_uint(dst[c]), __float_as_uint(dst[c + 1]),
-                    __float_as_uint(dst[c + 2]), __float_as_uint(dst[c + 3]), xb);
+      for (int c = 0; c < kBN / 4; ++c)
+        *reinterpret_cast<float4*>(srow + ((((uint32_t)c) ^ xsw) << 4)) =
+            make_float4(dst[4 * c], dst[4 * c + 1], dst[4 * c + 2], dst[4 * c + 3]);
+      fence_proxy_async_smem();
+      named_bar_sync(2, 128);                // all rows staged
+      if (i == 0) {
+        if (j >= 2) W.wait(bar(kBarXFree + buf), ((j >> 1) - 1) & 1);
+        bulk_copy_to_peer(x_peer + buf * kXBytes, sb + kOffXs, kXTxBytes, xfull_peer + 8u * buf);
+        bulk_commit_group();
+      }
     };
 
     float sp[kBN], nx[kBN];
@@ -426,11 +439,11 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
       if (b + 1 < nb) load_and_send(b + 1, nx);
       // The peer's partial for this block; then let the peer reuse the buffer.
       W.wait_cluster(bar(kBarXFull + buf), (b >> 1) & 1);
-      const float* xr = Xs + buf * (kXBytes / 4) + i * kXStride;
+      const uint8_t* xr = reinterpret_cast<const uint8_t*>(Xs) + buf * kXBytes + xrow;
 #pragma unroll
-      for (int c = 0; c < kBN; c += 4) {
-        const float4 x = *reinterpret_cast<const float4*>(xr + c);
-        sp[c] += x.x; sp[c + 1] += x.y; sp[c + 2] += x.z; sp[c + 3] += x.w;
+      for (int c = 0; c < kBN / 4; ++c) {
+        const float4 x = *reinterpret_cast<const float4*>(xr + ((((uint32_t)c) ^ xsw) << 4));
+        sp[4 * c] += x.x; sp[4 * c + 1] += x.y; sp[4 * c + 2] += x.z; sp[4 * c + 3] += x.w;
       }
       mbar_arrive(bar(kBarXCons + buf));   // the signal warp tells the peer
       // a5: masked online softmax (log2 domain).
@@ -463,9 +476,9 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
         }
       }
       l_run = l_run * alpha + lsum;
-      if (b >= 2) W.wait(bar(kBarPEmpty + buf), ((b >> 1) - 1) & 1);
+      if (b >= 1) W.wait(bar(kBarPEmpty), (b - 1) & 1);   // PV(b-1) has read P
       // P row (48 bf16 = 6 chunks of 16 B) into the 128-byte-swizzled buffer.
-      uint8_t* prow = sm + kOffP + buf * kPBytes + i * 128;
+      uint8_t* prow = sm + kOffP + i * 128;
 #pragma unroll
       for (int j = 0; j < kBN / 8; ++j) {
         const uint32_t off = ((uint32_t)j ^ ((uint32_t)i & 7u)) << 4;
@@ -475,7 +488,7 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
       fence_proxy_async_smem();
       if (b >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) rescale_o(alpha, b);
       tc_fence_before();
-      mbar_arrive(bar(kBarPFull + buf));
+      mbar_arrive(bar(kBarPFull));
     }
 
     // ---- a7: epilogue ---------------------------------------------------------
@@ -537,6 +550,7 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
   // The peer's last X-free arrivals land asynchronously: wait for the final
   // phases of both X-free barriers first.
   if (tid == 128 && nb > 0) {
+    bulk_wait_read_all();
     if (nb >= 2) W.wait(bar(kBarXFree + ((nb - 2) & 1)), ((nb - 2) >> 1) & 1);
     W.wait(bar(kBarXFree + ((nb - 1) & 1)), ((nb - 1) >> 1) & 1);
   }

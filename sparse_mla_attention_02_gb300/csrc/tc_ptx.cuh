@@ -151,6 +151,24 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int 
       : "memory");
 }
 
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to
+// another CTA's, counted on that CTA's mbarrier (complete_tx).
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src_cta,
+                                                  uint32_t bytes, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst_cluster),
+      "r"(src_cta), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until every committed bulk copy of this thread has read its source.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // Asynchronous 16-byte store into another CTA's shared memory; its bytes are
 // counted on that CTA's mbarrier (complete_tx), which the receiver arms with
 // the expected byte count.
