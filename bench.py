@@ -314,7 +314,7 @@ def run_ours(args, rank, world, local_rank):
     # ---- secondary: bf16 decode ----------------------------------------------
     secondary = {}
     if not args.no_secondary:
-        for name in ["bf16_decode"]:
+        for name in ["bf16_decode", "fp8_nope_decode", "mixed_fp8_group"]:
             w2, ws2, out2, lse2, n2 = setup(name, rank)
             f2 = step_fn(w2, ws2, out2, lse2)
             with torch.cuda.stream(stream):
@@ -322,7 +322,7 @@ def run_ours(args, rank, world, local_rank):
                     f2()
             stream.synchronize()
             barrier()
-            k2 = max(args.steps, 20)
+            k2 = max(args.steps, 20) if name != "mixed_fp8_group" else max(3, args.steps)
             el2 = max_over_ranks(time_steps(f2, k2, stream))
             fl2 = flops_of(w2)
             U2, G2 = bytes_model(w2)
@@ -336,7 +336,7 @@ def run_ours(args, rank, world, local_rank):
                 "roofline_frac": round(max(fl2 / (pk["bf16_tflops"] * 1e12),
                                            U2 / (pk["hbm_gbs"] * 1e9)) / t2, 4),
                 "splits_workspace_bytes": n2,
-                "l2": "pool 2.4 GB > L2",
+                "kernel": "tcgen05" if w2.kv_dtype != W.KV_FP8_E4M3_GROUP128 else "cuda-core",
             }
             del w2, ws2, out2, lse2
             torch.cuda.empty_cache()

@@ -106,10 +106,12 @@ static_assert(kAtomBytes % 1024 == 0, "swizzle atoms must stay 1024-aligned");
 static_assert(kBN % 12 == 0, "three producer warps split the 4-row groups evenly");
 
 struct TcArgs {
-  CUtensorMap kv_map;  // the cache as a 2-D tensor [num_slots, d_qk], 64-channel boxes
+  CUtensorMap kv_map;  // bf16 cache as a 2-D tensor [num_slots, d_qk], 64-channel boxes
   FwdParams p;
+  int fp8;          // 1: E4M3 cache with a per-tensor scale (converted on load)
   int g_lo[2];      // first cache channel gathered by CTA r
-  int n_boxes[2];   // 64-channel boxes gathered per row by CTA r
+  int n_boxes[2];   // 64-channel boxes gathered per row by CTA r (bf16)
+  int n_chunks8[2]; // 16-byte FP8 chunks gathered per row by CTA r (fp8)
   int qk_lo[2];     // first local channel of CTA r's QK range
   int q_lo[2];      // first q channel CTA r keeps in TMEM
   int ksteps;       // 16-channel MMA steps of the QK half
@@ -144,6 +146,25 @@ struct Waiter {
   }
 };
 
+// Four E4M3 bytes -> four bf16 (two bf16x2 words), exactly: every E4M3 value
+// is a bf16 value.  The byte's exponent and mantissa fields are placed in the
+// bf16 fields (which reads the value times 2^-120, bias 7 vs 127; E4M3
+// subnormals land on bf16 subnormals), then one exact bf16 multiply by 2^120
+// restores it.  The E4M3 NaN code is not special-cased (the generator never
+// writes it).
+__device__ __forceinline__ uint32_t e4m3x2_lanes_to_bf16x2(uint32_t x) {
+  // x holds one byte in the low byte of each 16-bit lane
+  uint32_t bits = ((x & 0x007F007Fu) << 4) | ((x & 0x00800080u) << 8);
+  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&bits);
+  const uint32_t k2 = 0x7B807B80u;                 // (2^120, 2^120) in bf16
+  v = __hmul2(v, *reinterpret_cast<const __nv_bfloat162*>(&k2));
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ void e4m3x4_to_bf16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  lo = e4m3x2_lanes_to_bf16x2(__byte_perm(w, 0u, 0x4140u));   // bytes 0, 1
+  hi = e4m3x2_lanes_to_bf16x2(__byte_perm(w, 0u, 0x4342u));   // bytes 2, 3
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -177,7 +198,8 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(kBarKvFull + s), 3);      // one expect_tx per producer warp
+      // bf16: one expect_tx per TMA warp; fp8: one arrival per converter thread
+      mbar_init(bar(kBarKvFull + s), a.fp8 ? kProducers : 3);
       mbar_init(bar(kBarKvEmpty + s), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -303,6 +325,51 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
     // operand layout, and a masked position (slot id -1) reads the
     // out-of-bounds fill, i.e. a zero row.
     const int g_lo = a.g_lo[r];
+    if (a.fp8) {
+      // a2 + a3 for an E4M3 cache: two threads per row load the row's bytes
+      // with 16-byte loads (all loads of a block in flight at once), convert
+      // them exactly to bf16 and store the 128-byte-swizzled tile; masked
+      // rows are zero.  The per-tensor scale is applied in fp32 later (score
+      // scale and output normalization), so the tile holds exact values.
+      const int pt = tid - 32;
+      const int row = pt >> 1, half = pt & 1;
+      const uint32_t sw = (uint32_t)row & 7u;
+      const int nc8 = a.n_chunks8[r];                         // <= 20
+      const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
+      for (int b = 0; b < nb; ++b) {
+        const int s = b % kStages;
+        if (b >= kStages) W.wait(bar(kBarKvEmpty + s), ((b / kStages) - 1) & 1);
+        const int id = slots[b * kBN + row];
+        const uint4* src = reinterpret_cast<const uint4*>(
+            kv8 + (size_t)(id < 0 ? 0 : id) * p.d_qk + g_lo);
+        uint4 raw[10];
+#pragma unroll
+        for (int kk = 0; kk < 10; ++kk) {
+          const int c = half + 2 * kk;
+          raw[kk] = (id >= 0 && c < nc8) ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        uint8_t* rgen = sm + kOffTile + s * kTileBytes + row * 128;
+#pragma unroll
+        for (int kk = 0; kk < 10; ++kk) {
+          const int c = half + 2 * kk;
+          if (c < nc8) {
+            uint32_t o[8];
+            e4m3x4_to_bf16(raw[kk].x, o[0], o[1]);
+            e4m3x4_to_bf16(raw[kk].y, o[2], o[3]);
+            e4m3x4_to_bf16(raw[kk].z, o[4], o[5]);
+            e4m3x4_to_bf16(raw[kk].w, o[6], o[7]);
+            const uint32_t cj = 2u * (uint32_t)c;             // two bf16 chunks
+            *reinterpret_cast<uint4*>(rgen + (cj >> 3) * kAtomBytes + (((cj & 7u) ^ sw) << 4)) =
+                make_uint4(o[0], o[1], o[2], o[3]);
+            const uint32_t cj1 = cj + 1u;
+            *reinterpret_cast<uint4*>(rgen + (cj1 >> 3) * kAtomBytes + (((cj1 & 7u) ^ sw) << 4)) =
+                make_uint4(o[4], o[5], o[6], o[7]);
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kBarKvFull + s));
+      }
+    } else {
     const int n_boxes = a.n_boxes[r];
     const int w = warp - 1;                                   // 0..2
     const uint32_t tx_bytes = (uint32_t)(kBN / 4 / 3 * n_boxes * 512);
@@ -323,6 +390,7 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
         }
       }
       __syncwarp();
+    }
     }
   } else if (warp == 8) {
     // ---- signal warp: tell the peer when its partial scores were consumed --
@@ -367,6 +435,9 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
       tc_fence_before();
       mbar_arrive(bar(kBarQReady));
     }
+    // E4M3 cache: the per-tensor scale multiplies every score and output.
+    const float kscale = a.fp8 ? __ldg(p.k_scale) : 1.f;
+    const float scale_log2 = a.scale_log2 * kscale;
     float m_run = -INFINITY;   // running max (log2 units)
     float l_run = 0.f;         // running sum of exp2(s - m_run)
     const float* Xs = reinterpret_cast<const float*>(sm + kOffX);
@@ -452,7 +523,7 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
 #pragma unroll
       for (int j = 0; j < kBN; ++j) {
         const bool ok = ((j < 32 ? m_lo >> j : m_hi >> (j - 32)) & 1u) != 0u;
-        sp[j] = ok ? sp[j] * a.scale_log2 : -INFINITY;
+        sp[j] = ok ? sp[j] * scale_log2 : -INFINITY;
         bmax = fmaxf(bmax, sp[j]);
       }
       float alpha = 1.f;
@@ -499,7 +570,7 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
       tc_fence_after();
     }
     const bool empty = !(l_run > 0.f) || nb == 0;
-    const float inv = empty ? 0.f : 1.f / l_run;
+    const float inv = empty ? 0.f : kscale / l_run;
     const bool live = head < p.h;          // pad rows past h are not written
     const int64_t orow = (int64_t)t * p.h + (live ? head : 0);
     // Every lane of the warpgroup runs the TMEM loads (warp-collective);
@@ -571,7 +642,8 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
 int tc_max_range() { return kMaxBlocks * kBN; }
 
 bool tc_supported(int h, int d_qk, int kv_format) {
-  return h >= 1 && h <= 128 && (d_qk == 576 || d_qk == 512) && kv_format == kBf16;
+  return h >= 1 && h <= 128 && (d_qk == 576 || d_qk == 512) &&
+         (kv_format == kBf16 || kv_format == kE4m3);
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once through the runtime
@@ -593,24 +665,29 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 cudaError_t launch_tc(const FwdParams& p, cudaStream_t stream) {
   TcArgs a{};
   a.p = p;
-  auto encode = tensor_map_encoder();
-  if (!encode) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {(cuuint64_t)p.d_qk, (cuuint64_t)p.num_slots};
-  const cuuint64_t strides[1] = {(cuuint64_t)p.d_qk * 2};
-  const cuuint32_t box[2] = {64, 1};
-  const cuuint32_t estr[2] = {1, 1};
-  if (encode(&a.kv_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.kv), dims,
-             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
+  a.fp8 = p.kv_format == kE4m3 ? 1 : 0;
+  if (!a.fp8) {
+    auto encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)p.d_qk, (cuuint64_t)p.num_slots};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.d_qk * 2};
+    const cuuint32_t box[2] = {64, 1};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&a.kv_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.kv), dims,
+               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   if (p.d_qk == 576) {
     a.g_lo[0] = 0;   a.n_boxes[0] = 5; a.qk_lo[0] = 0;  a.q_lo[0] = 0;
     a.g_lo[1] = 256; a.n_boxes[1] = 5; a.qk_lo[1] = 32; a.q_lo[1] = 288;
+    a.n_chunks8[0] = 18; a.n_chunks8[1] = 20;   // channels 0..287, 256..575
     a.ksteps = 18;
   } else {
     a.g_lo[0] = 0;   a.n_boxes[0] = 4; a.qk_lo[0] = 0; a.q_lo[0] = 0;
     a.g_lo[1] = 256; a.n_boxes[1] = 4; a.qk_lo[1] = 0; a.q_lo[1] = 256;
+    a.n_chunks8[0] = 16; a.n_chunks8[1] = 16;   // channels 0..255, 256..511
     a.ksteps = 16;
   }
   a.scale_log2 = p.sm_scale * 1.4426950408889634f;

@@ -150,6 +150,33 @@ def test_scattered_minus_one_and_out_of_range(cuda_lib, kv_dtype):
     check(cuda_lib, w, valid=False)
 
 
+@pytest.mark.parametrize("h", [16, 128])
+def test_fp8_decode_every_code_exactly(cuda_lib, h):
+    """E4M3 cache rows holding every non-NaN code (subnormals included), one
+    key per token, k_scale = 1: O must equal the codes' values exactly
+    (every E4M3 value is a bf16 value and the softmax weight is exactly 1);
+    torch's float8_e4m3fn -> bf16 cast is the independent decoder."""
+    codes = torch.tensor([c for c in range(256) if c not in (0x7F, 0xFF)],
+                         dtype=torch.uint8)
+    S, d = 8, 576
+    kv = codes.repeat((S * d) // codes.numel() + 1)[: S * d].view(S, d).clone()
+    for srow in range(S):                      # a different code order per row
+        kv[srow] = kv[srow].roll(37 * srow)
+    T = S
+    w = W.custom(T=T, h=h, topk=4, num_slots=S, kv_dtype=1, k_scale=1.0,
+                 valid=[1] * T, seed=70)
+    w.kv = kv
+    w.k_scale = torch.tensor([1.0])
+    w.indices[:, 0] = torch.arange(T, dtype=torch.int32)
+    wd = w.to("cuda")
+    O, L = gpu_fwd(cuda_lib, wd)
+    ref = kv[:, :512].view(torch.float8_e4m3fn).to(torch.bfloat16)
+    for t in range(T):
+        assert torch.equal(O[t].cpu(), ref[t].unsqueeze(0).expand(h, 512)), t
+    Or, Lr = oracle_fwd(w)
+    compare(O, L, Or, Lr, "fp8_codes")
+
+
 def test_duplicate_indices(cuda_lib):
     w = W.custom(T=4, h=16, topk=64, num_slots=20, valid=[64, 30, 5, 1],
                  seed=37, distinct=False, name="duplicates")
