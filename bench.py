@@ -160,8 +160,25 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def make(name, device):
-    return W.CONFIGS[name](device=device)
+def workload_seed(name: str, rank: int) -> int:
+    """Each rank draws its own replica of the workload (independent problems,
+    weak scaling): same recipe, a different seed per rank."""
+    return 1000 + list(W.CONFIGS).index(name) + 7919 * rank
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest rank's time (the job is done when every rank is done)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, steps: int, t_max: float) -> float:
+    """Whole-job rate: every rank's units over the slowest rank's time."""
+    return world * units_per_rank * steps / t_max
 
 
 def time_steps(fn, steps, stream):
@@ -187,9 +204,8 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.Stream(dev)
     pk, pk_src = peaks()
 
-    def setup(name, seed_shift, tokens=0):
-        w = W.CONFIGS[name](device=dev, seed=1000 + list(W.CONFIGS).index(name)
-                            + 7919 * seed_shift)
+    def setup(name, rank_, tokens=0):
+        w = W.CONFIGS[name](device=dev, seed=workload_seed(name, rank_))
         if tokens and tokens < w.T:
             # the last `tokens` tokens (same kernel, a smaller launch)
             w = W.token_subset(w, np.arange(w.T - tokens, w.T), device=dev)
@@ -210,12 +226,8 @@ def run_ours(args, rank, world, local_rank):
         if world > 1:
             dist.barrier()
 
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    def ranks_max(x):
+        return max_over_ranks(x, world, dev)
 
     # ---- headline: bf16 prefill --------------------------------------------
     w, ws, out, lse, ws_n = setup(args.config, rank, args.tokens)
@@ -233,11 +245,11 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize(dev)
     barrier()
     clocks = cs.summary()
-    t_max = max_over_ranks(elapsed)
+    t_max = ranks_max(elapsed)
     ms = 1e3 * t_max / args.steps
     launches_per_step = 1 + (1 if ws_n > 0 else 0)
-    value = world * fl * args.steps / t_max / 1e12
-    tok_s = world * w.T * args.steps / t_max
+    value = job_throughput(fl, world, args.steps, t_max) / 1e12
+    tok_s = job_throughput(w.T, world, args.steps, t_max)
     kernel_s = elapsed / args.steps
     achieved = fl / kernel_s / 1e12
     bound_tensor = fl / (pk["bf16_tflops"] * 1e12) >= U / (pk["hbm_gbs"] * 1e9)
@@ -291,7 +303,7 @@ def run_ours(args, rank, world, local_rank):
     stream.synchronize()
     e2e_steps = max(3, args.steps // 2)
     barrier()
-    e2e_el = max_over_ranks(time_steps(e2e_step, e2e_steps, stream))
+    e2e_el = ranks_max(time_steps(e2e_step, e2e_steps, stream))
     h2d = h_q.numel() * 2 + h_idx.numel() * 4 + h_vl.numel() * 4
     d2h = h_out.numel() * 2 + h_lse.numel() * 4
     e2e = {"value": round(world * fl * e2e_steps / e2e_el / 1e12, 3),
@@ -323,7 +335,7 @@ def run_ours(args, rank, world, local_rank):
             stream.synchronize()
             barrier()
             k2 = max(args.steps, 20) if name != "mixed_fp8_group" else max(3, args.steps)
-            el2 = max_over_ranks(time_steps(f2, k2, stream))
+            el2 = ranks_max(time_steps(f2, k2, stream))
             fl2 = flops_of(w2)
             U2, G2 = bytes_model(w2)
             t2 = el2 / k2
