@@ -115,6 +115,27 @@ SMLA_API smla_status smla_fwd(const void* q, const void* kv_cache, int kv_dtype,
 SMLA_API size_t smla_workspace_size(int T, int h, int d_qk, int d_v, int topk,
                            int kv_dtype);
 
+/* Kernel families a plan can choose (see smla_plan_info). */
+typedef enum {
+  SMLA_KERNEL_CUDA_CORE = 0,     /* fp32 CUDA-core kernel (any supported shape) */
+  SMLA_KERNEL_TC_HEADS = 1,      /* tcgen05, heads as the MMA rows (h <= 128) */
+  SMLA_KERNEL_TC_KEYS = 2        /* tcgen05, top-k positions as the MMA rows (h <= 16) */
+} smla_kernel;
+
+/*
+ * smla_plan_info — how smla_fwd would run this shape on the current device:
+ * the kernel family (*kernel, an smla_kernel), the number of top-k ranges
+ * per token (*splits; > 1 means partial results merged by smla_combine's
+ * kernel) and the workspace that needs (*workspace_bytes).  Any output
+ * pointer may be NULL.  Host-only: launches nothing.  An inspection aid with
+ * no counterpart in the pages.  Errors: SMLA_ERR_INVALID_ARG /
+ * SMLA_ERR_UNSUPPORTED for shapes smla_fwd rejects, SMLA_ERR_CUDA when the
+ * device cannot be queried.
+ */
+SMLA_API smla_status smla_plan_info(int T, int h, int d_qk, int d_v, int topk,
+                                    int kv_dtype, int* kernel, int* splits,
+                                    size_t* workspace_bytes);
+
 /*
  * smla_fwd_ws — smla_fwd with a caller-owned device workspace of at least
  * smla_workspace_size(...) bytes (256-byte aligned; NULL allowed when that

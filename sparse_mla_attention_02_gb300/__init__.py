@@ -60,6 +60,9 @@ def load():
         lib.smla_fwd_ws.restype = I
         lib.smla_workspace_size.argtypes = [I, I, I, I, I, I]
         lib.smla_workspace_size.restype = SZ
+        lib.smla_plan_info.argtypes = [I, I, I, I, I, I, ctypes.POINTER(I),
+                                       ctypes.POINTER(I), ctypes.POINTER(SZ)]
+        lib.smla_plan_info.restype = I
         lib.smla_combine.argtypes = [P, P, I, I64, I, P, P, P]
         lib.smla_combine.restype = I
         lib.smla_get_device_status.argtypes = [ctypes.POINTER(I), I]
@@ -140,6 +143,20 @@ def smla_fwd(q, kv_cache, kv_dtype, k_scale, indices, valid_len, sm_scale,
 
 def smla_workspace_size(T, h, d_qk, topk, kv_dtype, d_v=512) -> int:
     return int(load().smla_workspace_size(T, h, d_qk, d_v, topk, kv_dtype))
+
+
+KERNEL_NAMES = {0: "cuda_core", 1: "tc_heads", 2: "tc_keys"}
+
+
+def smla_plan_info(T, h, d_qk, topk, kv_dtype, d_v=512) -> dict:
+    """``smla_plan_info``: the kernel family, top-k splits and workspace a
+    forward of this shape uses on the current device."""
+    lib = load()
+    k, s, n = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_size_t(0)
+    _check(lib.smla_plan_info(T, h, d_qk, d_v, topk, kv_dtype, ctypes.byref(k),
+                              ctypes.byref(s), ctypes.byref(n)), "smla_plan_info")
+    return {"kernel": KERNEL_NAMES[k.value], "splits": s.value,
+            "workspace_bytes": n.value}
 
 
 def smla_fwd_ws(q, kv_cache, kv_dtype, k_scale, indices, valid_len, sm_scale,

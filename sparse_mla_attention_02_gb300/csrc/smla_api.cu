@@ -134,9 +134,9 @@ smla_status run_fwd(const void* q, const void* kv, int kv_dtype,
     p.o_part = static_cast<float*>(ws);
     p.lse_part = p.o_part + (size_t)plan.splits * T * h * d_v;
   }
-  const cudaError_t le = plan.kind == smla::kKernelTc
-                            ? smla::launch_tc(p, stream)
-                            : smla::launch_simt(p, stream);
+  const cudaError_t le = plan.kind == smla::kKernelTcKeys ? smla::launch_tc_keys(p, stream)
+                         : plan.kind == smla::kKernelTc   ? smla::launch_tc(p, stream)
+                                                          : smla::launch_simt(p, stream);
   if (le != cudaSuccess) return SMLA_ERR_CUDA;
   if (plan.splits > 1) {
     if (smla::launch_combine(p.o_part, p.lse_part, plan.splits, (int64_t)T * h,
@@ -153,18 +153,22 @@ namespace smla {
 // Split plan.  Valid counts are device data, so ranges are cut over topk; a
 // range past a token's valid count yields an empty partial (0, -inf) that the
 // combine ignores.
-//  - tensor-core path: one unit = (token, range) on a 2-SM cluster, one
-//    cluster per two SMs resident; split only when the tokens alone leave
-//    more than half of the pairs idle (each split costs partial-O traffic).
+//  - tensor-core paths (keys-major for h <= 16, heads-major up to 128): one
+//    unit = (token, range) on a 2-SM cluster, one cluster per two SMs
+//    resident; split only when the tokens alone leave more than half of the
+//    pairs idle (each split costs partial-O traffic), or when topk is longer
+//    than one unit's range.
 //  - CUDA-core path: enough (token, 16-head group, range) units to fill every
 //    SM twice.
 Plan make_plan(int T, int h, int d_qk, int d_v, int topk, int kv_format,
                int num_sms) {
   Plan pl{};
   int splits = 1, gran = 32;
-  if (tc_supported(h, d_qk, kv_format)) {
-    pl.kind = kKernelTc;
-    gran = 64;
+  const bool keys = tc_keys_supported(h, d_qk, kv_format);
+  if (keys || tc_supported(h, d_qk, kv_format)) {
+    pl.kind = keys ? kKernelTcKeys : kKernelTc;
+    gran = keys ? 128 : 64;
+    const int max_range = keys ? tc_keys_max_range() : tc_max_range();
     const int pairs = num_sms > 1 ? num_sms / 2 : 1;
     if (2LL * T < pairs) {
       splits = pairs / (T > 0 ? T : 1);
@@ -173,7 +177,7 @@ Plan make_plan(int T, int h, int d_qk, int d_v, int topk, int kv_format,
       if (splits > 16) splits = 16;
       if (splits < 1) splits = 1;
     }
-    const int need = (topk + tc_max_range() - 1) / tc_max_range();
+    const int need = (topk + max_range - 1) / max_range;
     if (splits < need) splits = need;
   } else {
     pl.kind = kKernelSimt;
@@ -233,6 +237,29 @@ size_t smla_workspace_size(int T, int h, int d_qk, int d_v, int topk,
   }
   return smla::make_plan(T, h, d_qk, d_v, topk, kv_dtype, dev->num_sms)
       .workspace_bytes;
+}
+
+smla_status smla_plan_info(int T, int h, int d_qk, int d_v, int topk,
+                           int kv_dtype, int* kernel, int* splits,
+                           size_t* workspace_bytes) {
+  if (T < 1 || h < 1 || topk < 1) return SMLA_ERR_INVALID_ARG;
+  if (h > 128 || (d_qk != 512 && d_qk != 576) || d_v != 512 ||
+      kv_dtype < SMLA_KV_BF16 || kv_dtype > SMLA_KV_FP8_E4M3_GROUP128)
+    return SMLA_ERR_UNSUPPORTED;
+  DeviceInfo* dev = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    const smla_status st = device_info(&dev);
+    if (st != SMLA_OK) return st;
+  }
+  const smla::Plan pl = smla::make_plan(T, h, d_qk, d_v, topk, kv_dtype, dev->num_sms);
+  if (kernel)
+    *kernel = pl.kind == smla::kKernelTcKeys ? SMLA_KERNEL_TC_KEYS
+              : pl.kind == smla::kKernelTc   ? SMLA_KERNEL_TC_HEADS
+                                             : SMLA_KERNEL_CUDA_CORE;
+  if (splits) *splits = pl.splits;
+  if (workspace_bytes) *workspace_bytes = pl.workspace_bytes;
+  return SMLA_OK;
 }
 
 smla_status smla_combine(const float* o_parts, const float* lse_parts,

@@ -35,7 +35,7 @@ struct FwdParams {
 };
 
 // Which kernel family a plan uses.
-enum KernelKind { kKernelSimt = 0, kKernelTc = 1 };
+enum KernelKind { kKernelSimt = 0, kKernelTc = 1, kKernelTcKeys = 2 };
 
 struct Plan {
   int kind;
@@ -51,6 +51,10 @@ cudaError_t launch_simt(const FwdParams& p, cudaStream_t stream);
 bool tc_supported(int h, int d_qk, int kv_format);
 int tc_max_range();  // largest top-k range one tensor-core unit covers
 cudaError_t launch_tc(const FwdParams& p, cudaStream_t stream);
+// Keys-major tensor-core kernel for h <= 16 (all formats, incl. group scales).
+bool tc_keys_supported(int h, int d_qk, int kv_format);
+int tc_keys_max_range();
+cudaError_t launch_tc_keys(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_combine(const float* o_parts, const float* lse_parts,
                            int n_parts, int64_t rows, int d_v, void* out,
                            float* lse, cudaStream_t stream);

@@ -48,6 +48,7 @@
 #include <mutex>
 
 #include "smla_internal.h"
+#include "tc_common.cuh"
 #include "tc_ptx.cuh"
 
 namespace smla {
@@ -117,58 +118,6 @@ struct TcArgs {
   int ksteps;       // 16-channel MMA steps of the QK half
   float scale_log2; // sm_scale * log2(e)
 };
-
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-// Bounded waits.  A wait that runs out (or sees that another block already
-// gave up) records the timeout status, sets this block's abort flag, and from
-// then on every wait of the block returns at once, so the block still reaches
-// its teardown.  Results of an aborted launch are undefined; no access goes
-// out of bounds.
-struct Waiter {
-  volatile int* abort;
-  int* status;
-  __device__ __forceinline__ void fail() {
-    if (!*abort) {
-      *abort = 1;
-      atomicCAS(status, 0, kStatusTimeout);
-    }
-  }
-  __device__ __forceinline__ void wait(uint32_t bar, uint32_t parity) {
-    if (*abort) return;
-    if (!mbar_wait_bounded<false>(bar, parity, status, kStatusTimeout)) fail();
-  }
-  __device__ __forceinline__ void wait_cluster(uint32_t bar, uint32_t parity) {
-    if (*abort) return;
-    if (!mbar_wait_bounded<true>(bar, parity, status, kStatusTimeout)) fail();
-  }
-};
-
-// Four E4M3 bytes -> four bf16 (two bf16x2 words), exactly: every E4M3 value
-// is a bf16 value.  The byte's exponent and mantissa fields are placed in the
-// bf16 fields (which reads the value times 2^-120, bias 7 vs 127; E4M3
-// subnormals land on bf16 subnormals), then one exact bf16 multiply by 2^120
-// restores it.  The E4M3 NaN code is not special-cased (the generator never
-// writes it).
-__device__ __forceinline__ uint32_t e4m3x2_lanes_to_bf16x2(uint32_t x) {
-  // x holds one byte in the low byte of each 16-bit lane
-  uint32_t bits = ((x & 0x007F007Fu) << 4) | ((x & 0x00800080u) << 8);
-  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&bits);
-  const uint32_t k2 = 0x7B807B80u;                 // (2^120, 2^120) in bf16
-  v = __hmul2(v, *reinterpret_cast<const __nv_bfloat162*>(&k2));
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-__device__ __forceinline__ void e4m3x4_to_bf16(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  lo = e4m3x2_lanes_to_bf16x2(__byte_perm(w, 0u, 0x4140u));   // bytes 0, 1
-  hi = e4m3x2_lanes_to_bf16x2(__byte_perm(w, 0u, 0x4342u));   // bytes 2, 3
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 smla_tc_kernel(const __grid_constant__ TcArgs a) {
@@ -648,7 +597,7 @@ bool tc_supported(int h, int d_qk, int kv_format) {
 
 // cuTensorMapEncodeTiled from the driver, looked up once through the runtime
 // (the library does not link libcuda directly).
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -662,22 +611,29 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+cudaError_t encode_bf16_rows_map(CUtensorMap* map, const void* kv, int d_qk,
+                                 int64_t num_slots) {
+  auto encode = tensor_map_encoder();
+  if (!encode) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)d_qk, (cuuint64_t)num_slots};
+  const cuuint64_t strides[1] = {(cuuint64_t)d_qk * 2};
+  const cuuint32_t box[2] = {64, 1};
+  const cuuint32_t estr[2] = {1, 1};
+  if (encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv), dims,
+             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  return cudaSuccess;
+}
+
 cudaError_t launch_tc(const FwdParams& p, cudaStream_t stream) {
   TcArgs a{};
   a.p = p;
   a.fp8 = p.kv_format == kE4m3 ? 1 : 0;
   if (!a.fp8) {
-    auto encode = tensor_map_encoder();
-    if (!encode) return cudaErrorNotSupported;
-    const cuuint64_t dims[2] = {(cuuint64_t)p.d_qk, (cuuint64_t)p.num_slots};
-    const cuuint64_t strides[1] = {(cuuint64_t)p.d_qk * 2};
-    const cuuint32_t box[2] = {64, 1};
-    const cuuint32_t estr[2] = {1, 1};
-    if (encode(&a.kv_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.kv), dims,
-               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
+    const cudaError_t e = encode_bf16_rows_map(&a.kv_map, p.kv, p.d_qk, p.num_slots);
+    if (e != cudaSuccess) return e;
   }
   if (p.d_qk == 576) {
     a.g_lo[0] = 0;   a.n_boxes[0] = 5; a.qk_lo[0] = 0;  a.q_lo[0] = 0;

@@ -1,0 +1,88 @@
+// tc_common.cuh — device helpers shared by the two tensor-core kernels
+// (heads-major smla_tc.cu, keys-major smla_tc_keys.cu): bounded waits with a
+// per-block abort flag, exact E4M3 -> bf16 conversion, bf16 packing, named
+// barriers, and the bf16 cache tensor map used by TMA gathers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include "smla_internal.h"
+#include "tc_ptx.cuh"
+
+namespace smla {
+
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// OR of `pred` over the `n` threads that meet at named barrier `id`.
+__device__ __forceinline__ bool named_bar_or(int id, int n, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(out)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(n)
+      : "memory");
+  return out != 0u;
+}
+
+// Bounded waits.  A wait that runs out (or sees that another block already
+// gave up) records the timeout status, sets this block's abort flag, and from
+// then on every wait of the block returns at once, so the block still reaches
+// its teardown.  Results of an aborted launch are undefined; no access goes
+// out of bounds.
+struct Waiter {
+  volatile int* abort;
+  int* status;
+  __device__ __forceinline__ void fail() {
+    if (!*abort) {
+      *abort = 1;
+      atomicCAS(status, 0, kStatusTimeout);
+    }
+  }
+  __device__ __forceinline__ void wait(uint32_t bar, uint32_t parity) {
+    if (*abort) return;
+    if (!ptx::mbar_wait_bounded<false>(bar, parity, status, kStatusTimeout)) fail();
+  }
+  __device__ __forceinline__ void wait_cluster(uint32_t bar, uint32_t parity) {
+    if (*abort) return;
+    if (!ptx::mbar_wait_bounded<true>(bar, parity, status, kStatusTimeout)) fail();
+  }
+};
+
+// Four E4M3 bytes -> four bf16 (two bf16x2 words), exactly: every E4M3 value
+// is a bf16 value.  The byte's exponent and mantissa fields are placed in the
+// bf16 fields (which reads the value times 2^-120, bias 7 vs 127; E4M3
+// subnormals land on bf16 subnormals), then one exact bf16 multiply by 2^120
+// restores it.  The E4M3 NaN code is not special-cased (the generator never
+// writes it).
+__device__ __forceinline__ uint32_t e4m3x2_lanes_to_bf16x2(uint32_t x) {
+  // x holds one byte in the low byte of each 16-bit lane
+  uint32_t bits = ((x & 0x007F007Fu) << 4) | ((x & 0x00800080u) << 8);
+  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&bits);
+  const uint32_t k2 = 0x7B807B80u;                 // (2^120, 2^120) in bf16
+  v = __hmul2(v, *reinterpret_cast<const __nv_bfloat162*>(&k2));
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ void e4m3x4_to_bf16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  lo = e4m3x2_lanes_to_bf16x2(__byte_perm(w, 0u, 0x4140u));   // bytes 0, 1
+  hi = e4m3x2_lanes_to_bf16x2(__byte_perm(w, 0u, 0x4342u));   // bytes 2, 3
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// A bf16 cache [num_slots, d_qk] as a 2-D tensor with 64-channel x 1-row
+// boxes and the 128-byte swizzle of the MMA operand tiles (TMA tile::gather4
+// reads four such rows per instruction; a row id of -1 reads zeros).
+cudaError_t encode_bf16_rows_map(CUtensorMap* map, const void* kv, int d_qk,
+                                 int64_t num_slots);
+
+}  // namespace smla

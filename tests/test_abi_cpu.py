@@ -27,7 +27,8 @@ def declared_symbols():
 def test_header_declares_the_boundary():
     names = declared_symbols()
     for n in ["smla_fwd", "smla_fwd_ws", "smla_workspace_size", "smla_combine",
-              "smla_get_device_status", "smla_status_string", "smla_version"]:
+              "smla_get_device_status", "smla_status_string", "smla_version",
+              "smla_plan_info"]:
         assert n in names
 
 
@@ -88,3 +89,17 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(build, "LIB", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         smla.load()
+
+
+def test_plan_info_argument_checks(lib):
+    """Shape errors are reported before any device query."""
+    k, n = ctypes.c_int(-1), ctypes.c_size_t(0)
+    q = lambda *a: lib.smla_plan_info(*a, ctypes.byref(k), None, ctypes.byref(n))
+    assert q(0, 16, 576, 512, 64, 0) == 1
+    assert q(4, 0, 576, 512, 64, 0) == 1
+    assert q(4, 16, 576, 512, 0, 0) == 1
+    assert q(4, 129, 576, 512, 64, 0) == 2
+    assert q(4, 16, 640, 512, 64, 0) == 2
+    assert q(4, 16, 576, 256, 64, 0) == 2
+    assert q(4, 16, 576, 512, 64, 3) == 2
+    assert k.value == -1                      # outputs untouched on error
