@@ -8,9 +8,9 @@
 //   S^T[keys, heads] = K[keys, d] . Q^T[d, heads]         A = gathered tile, K-major
 //   O^T[ch, heads]  += V^T[ch, keys] . P^T[keys, heads]    A = the same tile, MN-major
 // One work unit = (query token, top-k range) on a cluster of two CTAs that
-// split the channels at 256, a 128-channel group boundary: CTA 0 holds
-// channels [0, 256) (groups 0, 1), CTA 1 holds [256, d_qk) (groups 2, 3 and,
-// for d_qk = 576, the 64-channel rope group 4).
+// split the channels: CTA r holds channels [256r, 256r + 256) (groups 2r and
+// 2r + 1) and, for d_qk = 576, half of the 64-channel rope group 4,
+// [512 + 32r, 544 + 32r), so both CTAs gather and multiply the same bytes.
 //   * QK: with group scales each CTA keeps one fp32 accumulator per group in
 //     TMEM, so a key's group scale multiplies its partial score exactly (in
 //     fp32) before the groups are summed.  The CTA sends its partial scores
@@ -19,9 +19,11 @@
 //   * PV: CTA r owns output channels [256r, 256r + 256) = groups 2r, 2r + 1.
 //     With group scales, P^T is stored once per group, each key's entry
 //     multiplied by that key's group scale, so the tile keeps exact values.
-//     A scaled entry is kept as a bf16 pair hi + lo (two MMAs on the same V
-//     tile), so the scale costs no precision: a single bf16 rounding of
-//     p * scale would put up to 2^-9 relative error on O even for one key.
+//     A scaled entry is kept as a bf16 pair hi + lo, side by side in the N
+//     dimension (N = 32: the MMA's cost is set by reading its 4 KB A slice,
+//     so the wider N is free) and summed in the epilogue; a single bf16
+//     rounding of p * scale would put up to 2^-9 relative error on O even
+//     for one key.
 // Thread i of the softmax warpgroup owns key i of the block (TMEM lane i):
 // the key's group scales and valid bit are per-thread values, the per-head
 // max is reduced across the warpgroup only when some score passes the
@@ -42,12 +44,13 @@
 //      group scales applied per group accumulator (QK) and per copy of P (PV)
 //   a4 QK^T, a5 masked online softmax, a6 PV, a7 O / l and LSE = m + ln l
 //
-// Warp roles (320 threads): warp 0 issues MMAs and owns TMEM; warps 1..4
-// load the unit's slot ids, then gather (bf16: TMA; E4M3: one thread per key
-// row loads, converts and stores); warp 5 tells the peer when its partial
-// scores were consumed; warps 6..9 (thread <-> key <-> TMEM lane) load Q,
-// run the exchange, softmax, O rescale and the epilogue.  (Ten warps leave
-// each thread up to 168 registers.)
+// Warp roles (352 threads): warp 0 issues the QK MMAs and owns TMEM; warp 10
+// issues the PV MMAs; warps 1..4 load the unit's slot ids, then gather
+// (bf16: TMA; E4M3: one thread per key row loads, converts and stores);
+// warp 5 tells the peer when its partial scores were consumed; warps 6..9
+// (thread <-> key <-> TMEM lane) load Q, run the exchange, softmax, O
+// rescale and the epilogue.  (Eleven warps leave each thread up to 168
+// registers.)
 // Every wait is bounded; a wait that runs out records a timeout status, sets
 // an abort flag that skips later waits, and the block finishes normally.
 #include <math.h>
@@ -69,19 +72,21 @@ constexpr int kMaxChunks = 5;              // up to 320 channels per CTA
 constexpr int kStageBytes = kMaxChunks * kChunkBytes;
 constexpr int kScaleBytes = kBK * 16;      // 4 group-scale slots per key
 constexpr int kQChunkBytes = kN * 128;     // 64 channels x 16 heads
-constexpr int kPCopyBytes = 2 * kQChunkBytes;   // P^T copy: 16 heads x 128 keys
-constexpr int kPAreaBytes = 4 * kPCopyBytes;    // 2 buffers x 1 copy, or 1 x 4 (group)
+constexpr int kPCopyBytes = 2 * kQChunkBytes;   // P^T: 16 rows x 128 keys (2 K-atoms)
+constexpr int kPAreaBytes = 4 * kPCopyBytes;    // 2 buffers x 1 copy, or 2 groups x
+                                                // [hi | lo] rows (32 x 128 keys)
 constexpr int kXBytes = kBK * kN * 4;      // exchanged partial scores, fp32
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kProducers = 128;            // warps 1..4
 constexpr int kSoftmax = 128;              // warps 6..9
 constexpr int kMaxBlocks = 16;             // ranges up to 2048 positions
 
 // TMEM columns.
-constexpr uint32_t kColO = 0;              // O^T: 2 blocks of 128 channels x 16
-constexpr uint32_t kColS = 2 * kN;         // partial S: 2 buffers x 3 groups x 16
+constexpr uint32_t kColO = 0;              // O^T: 2 blocks of 128 channels x 32
+                                           // (16 heads, or hi | lo with group scales)
+constexpr uint32_t kColS = 4 * kN;         // partial S: 2 buffers x 3 groups x 16
 constexpr uint32_t kSBuf = 3 * kN;
-constexpr uint32_t kTmemCols = 128;
+constexpr uint32_t kTmemCols = 256;
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
 constexpr uint32_t kOffTile = 0;
@@ -120,7 +125,7 @@ static_assert(kColS + 2 * kSBuf <= kTmemCols, "TMEM budget");
 struct KeysArgs {
   CUtensorMap kv_map;  // bf16 cache as a 2-D tensor, 64-channel boxes (bf16 only)
   FwdParams p;
-  int n_chunks[2];     // 64-channel chunks of CTA r's channel range
+  int ksteps;          // 16-channel QK steps per CTA: 18 (d_qk 576) or 16 (512)
   int G;               // scale groups per slot (group format)
   float scale_log2;    // sm_scale * log2(e)
 };
@@ -160,6 +165,8 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
   // otherwise one copy, double-buffered.
   constexpr int kPBufs = kGroup ? 1 : 2;
   constexpr int kPBufBytes = kPAreaBytes / kPBufs;
+  constexpr int kPAtomBytes = kGroup ? 2 * kQChunkBytes : kQChunkBytes;  // one K-atom
+  constexpr int kNpv = kGroup ? 2 * kN : kN;                              // PV MMA N
   extern __shared__ uint8_t smem_raw[];
   const FwdParams& p = a.p;
   const uint32_t raw = smem_u32(smem_raw);
@@ -179,10 +186,12 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
   const int k1 = min(k0 + p.split_len, v);
   // The host plan keeps every range within kMaxBlocks blocks.
   const int nb = k1 > k0 ? min((k1 - k0 + kBK - 1) / kBK, kMaxBlocks) : 0;
-  const int n_chunks = a.n_chunks[r];
-  const int ksteps = 4 * n_chunks;                     // 16-channel MMA steps
+  // CTA r's channels: steps 0..15 = [256r, 256r + 256); steps 16, 17 (d_qk
+  // 576) = rope [512 + 32r, 544 + 32r), held in tile chunk 4.
+  const int ksteps = a.ksteps;
   const int n_lg = kGroup ? (ksteps + 7) / 8 : 1;       // group accumulators
-  const int g_lo = 256 * (int)r;                        // first channel of CTA r
+  const int g_lo = 256 * (int)r;                        // first V channel of CTA r
+  const int rope_lo = 512 + 32 * (int)r;                // first rope channel
 
   auto bar = [&](int i) { return sb + kOffBar + 8u * (uint32_t)i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffAbort);
@@ -247,16 +256,16 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
   __syncthreads();
 
   const bool leader = warp == 8 && lane == 0;            // softmax thread of key 0
-  if (warp == 0) {
-    // ---- MMA issuer ---------------------------------------------------------
-    // The whole warp runs this code (warp-uniform waits and descriptors); one
-    // elected lane issues each batch of MMAs and its commits.
+  if (warp == 0 || warp == 10) {
+    // ---- MMA issuers: warp 0 issues QK, warp 10 issues PV -------------------
+    // Two warps, each blocked only on its own inputs, so neither kind of
+    // batch waits behind the other.  Each warp runs its code warp-uniformly;
+    // one elected lane issues a batch of MMAs and commits it (a commit
+    // tracks the MMAs of the issuing thread).
     if (nb > 0) {
       const uint32_t id_qk = idesc_bf16(128, kN, false, false);
-      const uint32_t id_pv = idesc_bf16(128, kN, true, false);
+      const uint32_t id_pv = idesc_bf16(128, kNpv, true, false);
       const uint32_t qb = sb + kOffQ;
-      W.wait(bar(kBarQReady), 0);
-      tc_fence_after();
       auto issue_qk = [&](int j) {
         const int s = j & 1;
         W.wait(bar(kBarKvFull + s), (j >> 1) & 1);
@@ -267,13 +276,19 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
         const uint32_t dS = tmem + kColS + kSBuf * s;
         if (elect_one()) {
           fence_proxy_async_smem();
-          for (int ks = 0; ks < ksteps; ++ks) {
-            const uint32_t c = (uint32_t)(ks >> 2), ko = (uint32_t)(ks & 3) * 32u;
-            const uint32_t acc = kGroup ? (uint32_t)(ks >> 3) * kN : 0u;
-            const bool first = kGroup ? (ks & 7) == 0 : ks == 0;
-            mma_ss(dS + acc, sdesc(tile + c * kChunkBytes + ko, 16, 1024, kLayoutSw128),
-                   sdesc(qb + c * kQChunkBytes + ko, 16, 1024, kLayoutSw128), id_qk,
-                   first ? 0u : 1u);
+          // A descriptor's start-address field is addr >> 4 in its low bits,
+          // so each step's descriptor is the base plus a constant.
+          const uint64_t a0 = sdesc(tile, 16, 1024, kLayoutSw128);
+          const uint64_t b0 = sdesc(qb, 16, 1024, kLayoutSw128);
+#pragma unroll
+          for (int ks = 0; ks < 18; ++ks) {
+            if (ks < ksteps) {
+              const uint32_t oa = (uint32_t)((ks >> 2) * kChunkBytes + (ks & 3) * 32);
+              const uint32_t ob = (uint32_t)((ks >> 2) * kQChunkBytes + (ks & 3) * 32);
+              const uint32_t acc = kGroup ? (uint32_t)(ks >> 3) * kN : 0u;
+              const bool first = kGroup ? (ks & 7) == 0 : ks == 0;
+              mma_ss(dS + acc, a0 + (oa >> 4), b0 + (ob >> 4), id_qk, first ? 0u : 1u);
+            }
           }
           mma_commit(bar(kBarSFull + s));
         }
@@ -289,22 +304,21 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
         const uint32_t pb = sb + kOffP + pbi * kPBufBytes;
         if (elect_one()) {
           fence_proxy_async_smem();
+          // A = V^T: 128 channels (two 64-channel chunks) x 16 keys, MN-major;
+          // B = P^T of this channel group: 16 keys x N, K-major (group
+          // scales: rows 0..15 = hi, 16..31 = lo).
+          const uint64_t a0 = sdesc(tile, kChunkBytes, 1024, kLayoutSw128);
+          const uint64_t b0 = sdesc(pb, 16, 1024, kLayoutSw128);
+          const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
           for (int mb = 0; mb < 2; ++mb) {
 #pragma unroll
             for (int ks = 0; ks < kBK / 16; ++ks) {
-              // A = V^T: 128 channels (two 64-channel chunks) x 16 keys, MN-major
-              const uint64_t ad = sdesc(tile + 2 * mb * kChunkBytes + ks * 16 * 128,
-                                        kChunkBytes, 1024, kLayoutSw128);
-              // B = P^T copy of this channel group: 16 keys x 16 heads, K-major
-              // (group scales: the hi copy, then the lo copy)
-              const uint32_t bk = (ks >> 2) * kQChunkBytes + (ks & 3) * 32;
-              const uint32_t b0 = pb + (kGroup ? 2 * mb * kPCopyBytes : 0) + bk;
-              mma_ss(tmem + kColO + kN * mb, ad, sdesc(b0, 16, 1024, kLayoutSw128), id_pv,
-                     (j > 0 || ks > 0) ? 1u : 0u);
-              if (kGroup)
-                mma_ss(tmem + kColO + kN * mb, ad,
-                       sdesc(b0 + kPCopyBytes, 16, 1024, kLayoutSw128), id_pv, 1u);
+              const uint32_t oa = (uint32_t)(2 * mb * kChunkBytes + ks * 16 * 128);
+              const uint32_t ob = (uint32_t)((kGroup ? mb * 2 * kPAtomBytes : 0) +
+                                             (ks >> 2) * kPAtomBytes + (ks & 3) * 32);
+              mma_ss(tmem + kColO + 2 * kN * mb, a0 + (oa >> 4), b0 + (ob >> 4), id_pv,
+                     ks > 0 ? 1u : acc0);
             }
           }
           mma_commit(bar(kBarODone));
@@ -314,19 +328,12 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
         }
         __syncwarp();
       };
-      issue_qk(0);
-      for (int j = 0; j < nb; ++j) {
-        // Block j+1's scores first when its tile has already landed (keeps
-        // the softmax warps busy); otherwise PV first, which frees block j's
-        // stage for the gather of block j+2 sooner.
-        bool next_ready = false;
-        if (j + 1 < nb)
-          next_ready = __shfl_sync(0xffffffffu,
-                                   mbar_try_wait(bar(kBarKvFull + ((j + 1) & 1)),
-                                                 ((j + 1) >> 1) & 1) ? 1 : 0, 0) != 0;
-        if (next_ready) issue_qk(j + 1);
-        issue_pv(j);
-        if (j + 1 < nb && !next_ready) issue_qk(j + 1);
+      if (warp == 0) {
+        W.wait(bar(kBarQReady), 0);
+        tc_fence_after();
+        for (int j = 0; j < nb; ++j) issue_qk(j);
+      } else {
+        for (int j = 0; j < nb; ++j) issue_pv(j);
       }
     }
   } else if (warp <= 4) {
@@ -337,28 +344,30 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
       // the 128-byte-swizzled tile.  Masked rows are zero.
       const int row = tid - 32;
       const uint32_t sw = (uint32_t)row & 7u;
-      const int n_u = n_chunks * 4;                          // 16-byte pieces: 16 or 20
+      const int n_u = ksteps;                                // 16-byte pieces: 18 or 16
       const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
       for (int b = 0; b < nb; ++b) {
         const int s = b & 1;
         const int id = slots[b * kBK + row];
-        const uint4* src = reinterpret_cast<const uint4*>(
-            kv8 + (size_t)(id < 0 ? 0 : id) * p.d_qk + g_lo);
-        uint4 rw[20];
+        const uint8_t* rowp = kv8 + (size_t)(id < 0 ? 0 : id) * p.d_qk;
+        const uint4* src = reinterpret_cast<const uint4*>(rowp + g_lo);
+        const uint4* srope = reinterpret_cast<const uint4*>(rowp + rope_lo);
+        uint4 rw[18];
 #pragma unroll
-        for (int u = 0; u < 20; ++u)
-          rw[u] = (id >= 0 && u < n_u) ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
+        for (int u = 0; u < 18; ++u)
+          rw[u] = (id >= 0 && u < n_u) ? __ldg(u < 16 ? src + u : srope + (u - 16))
+                                       : make_uint4(0u, 0u, 0u, 0u);
         float sc[3] = {0.f, 0.f, 0.f};
         if (kGroup && id >= 0) {
-          const float* srow = p.k_scale + (int64_t)id * a.G + 2 * (int)r;
-#pragma unroll
-          for (int lg = 0; lg < 3; ++lg)
-            if (lg < n_lg) sc[lg] = __ldg(srow + lg);
+          const float* srow = p.k_scale + (int64_t)id * a.G;
+          sc[0] = __ldg(srow + 2 * (int)r);
+          sc[1] = __ldg(srow + 2 * (int)r + 1);
+          if (n_lg > 2) sc[2] = __ldg(srow + 4);
         }
         if (b >= kStages) W.wait(bar(kBarKvEmpty + s), ((b >> 1) - 1) & 1);
         uint8_t* rgen = sm + kOffTile + s * kStageBytes + row * 128;
 #pragma unroll
-        for (int u = 0; u < 20; ++u) {
+        for (int u = 0; u < 18; ++u) {
           if (u < n_u) {
             uint32_t o[8];
             e4m3x4_to_bf16(rw[u].x, o[0], o[1]);
@@ -382,7 +391,8 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
     } else {
       // bf16: warps 1..4 each issue 8 of the 32 four-row groups per block.
       const int w = warp - 1;
-      const uint32_t tx_bytes = (uint32_t)(8 * n_chunks * 512);
+      const int n_boxes = ksteps > 16 ? 5 : 4;               // + one rope box
+      const uint32_t tx_bytes = (uint32_t)(8 * n_boxes * 512);
       for (int b = 0; b < nb; ++b) {
         const int s = b & 1;
         if (b >= kStages) W.wait(bar(kBarKvEmpty + s), ((b >> 1) - 1) & 1);
@@ -394,9 +404,10 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
           const int* bs = slots + b * kBK;
           for (int g = w; g < kBK / 4; g += 4) {
             const int y0 = bs[4 * g], y1 = bs[4 * g + 1], y2 = bs[4 * g + 2], y3 = bs[4 * g + 3];
-            for (int c = 0; c < n_chunks; ++c)
-              tma_gather4(tile + c * kChunkBytes + 4 * g * 128, &a.kv_map, g_lo + 64 * c, y0,
-                          y1, y2, y3, full);
+            // (the rope box of CTA 1 runs past the row end: zero fill)
+            for (int c = 0; c < n_boxes; ++c)
+              tma_gather4(tile + c * kChunkBytes + 4 * g * 128, &a.kv_map,
+                          c < 4 ? g_lo + 64 * c : rope_lo, y0, y1, y2, y3, full);
           }
         }
         __syncwarp();
@@ -418,16 +429,17 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
     // Q (channels of this CTA, heads >= h zero) -> the QK B operand:
     // K-major, 64-channel chunks of 16 rows x 128 B, 128-byte swizzle.
     {
-      const int per_head = n_chunks * 8;                 // 16-byte pieces per head
-      const int total = kN * per_head;                   // <= 640
+      const int per_head = 2 * ksteps;                   // 16-byte pieces per head
+      const int total = kN * per_head;                   // <= 576
       const uint4* q4 = reinterpret_cast<const uint4*>(p.q);
       uint4 qv[5];
 #pragma unroll
       for (int k = 0; k < 5; ++k) {
         const int idx = i + kSoftmax * k;
         const int hd = idx / per_head, c16 = idx - hd * per_head;
+        const int ch = c16 < 32 ? g_lo + 8 * c16 : rope_lo + 8 * (c16 - 32);
         qv[k] = (idx < total && hd < p.h)
-                    ? __ldg(q4 + (((int64_t)t * p.h + hd) * p.d_qk + g_lo) / 8 + c16)
+                    ? __ldg(q4 + (((int64_t)t * p.h + hd) * p.d_qk + ch) / 8)
                     : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
@@ -455,7 +467,7 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
     float* red = reinterpret_cast<float*>(sm + kOffRed); // [16 heads][4 warps]
     // This key's byte offset inside a P^T copy (K-major, 128-byte swizzle):
     // K-atom (i / 64), 16-byte chunk ((i % 64) / 8) ^ (head % 8), element i % 8.
-    const uint32_t p_atom = (uint32_t)(i >> 6) * kQChunkBytes + (uint32_t)(i & 7) * 2u;
+    const uint32_t p_atom = (uint32_t)(i >> 6) * kPAtomBytes + (uint32_t)(i & 7) * 2u;
     const uint32_t p_chunk = (uint32_t)(i & 63) >> 3;
 
     for (int b = 0; b < nb; ++b) {
@@ -574,13 +586,14 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
           const uint32_t off = (uint32_t)(hd >> 3) * 1024u + (uint32_t)(hd & 7) * 128u +
                                ((p_chunk ^ (uint32_t)(hd & 7)) << 4);
           if (kGroup) {
+            // group g at g * 2 atoms; row hd = hi, row 16 + hd = lo (+2048 B)
             const float v0 = pe[hd] * scp0, v1 = pe[hd] * scp1;
             const __nv_bfloat16 h0 = __float2bfloat16_rn(v0), h1 = __float2bfloat16_rn(v1);
             *reinterpret_cast<__nv_bfloat16*>(pb + off) = h0;
-            *reinterpret_cast<__nv_bfloat16*>(pb + kPCopyBytes + off) =
+            *reinterpret_cast<__nv_bfloat16*>(pb + 2048 + off) =
                 __float2bfloat16_rn(v0 - __bfloat162float(h0));
-            *reinterpret_cast<__nv_bfloat16*>(pb + 2 * kPCopyBytes + off) = h1;
-            *reinterpret_cast<__nv_bfloat16*>(pb + 3 * kPCopyBytes + off) =
+            *reinterpret_cast<__nv_bfloat16*>(pb + 2 * kPAtomBytes + off) = h1;
+            *reinterpret_cast<__nv_bfloat16*>(pb + 2 * kPAtomBytes + 2048 + off) =
                 __float2bfloat16_rn(v1 - __bfloat162float(h1));
           } else {
             *reinterpret_cast<__nv_bfloat16*>(pb + off) = __float2bfloat16_rn(pe[hd]);
@@ -597,14 +610,15 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
         __syncwarp();
         tc_fence_after();
 #pragma unroll
-        for (int mb = 0; mb < 2; ++mb) {
+        for (int c = 0; c < (kGroup ? 4 : 2); ++c) {   // 16-column pieces (hi, lo)
+          const uint32_t col = kColO + (kGroup ? kN * c : 2 * kN * c);
           uint32_t w[16];
-          tmem_ld16(tmem + lane_base + kColO + kN * mb, w);
+          tmem_ld16(tmem + lane_base + col, w);
           tmem_wait_ld();
 #pragma unroll
           for (int hd = 0; hd < kN; ++hd)
             w[hd] = __float_as_uint(__uint_as_float(w[hd]) * alpha[hd]);
-          tmem_st16(tmem + lane_base + kColO + kN * mb, w);
+          tmem_st16(tmem + lane_base + col, w);
         }
         tmem_wait_st();
       }
@@ -633,6 +647,10 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
       tc_fence_after();
     }
     const float oscale = kFmt == kE4m3 ? kscale : 1.f;
+    float inv[kN];
+#pragma unroll
+    for (int hd = 0; hd < kN; ++hd)
+      inv[hd] = (!(l[hd] > 0.f) || nb == 0) ? 0.f : oscale / l[hd];
 #pragma unroll
     for (int mb = 0; mb < 2; ++mb) {
       uint32_t w[16];
@@ -640,15 +658,22 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
       for (int hd = 0; hd < kN; ++hd) w[hd] = 0u;
       __syncwarp();
       if (nb > 0) {
-        tmem_ld16(tmem + lane_base + kColO + kN * mb, w);
+        tmem_ld16(tmem + lane_base + kColO + 2 * kN * mb, w);
+        if (kGroup) {                                   // O = hi part + lo part
+          uint32_t w2[16];
+          tmem_ld16(tmem + lane_base + kColO + 2 * kN * mb + kN, w2);
+          tmem_wait_ld();
+#pragma unroll
+          for (int hd = 0; hd < kN; ++hd)
+            w[hd] = __float_as_uint(__uint_as_float(w[hd]) + __uint_as_float(w2[hd]));
+        }
         tmem_wait_ld();
       }
       const int ch = g_lo + 128 * mb + i;            // output channel of lane i
 #pragma unroll
       for (int hd = 0; hd < kN; ++hd) {
         if (hd < p.h) {
-          const bool empty = !(l[hd] > 0.f) || nb == 0;
-          const float o = empty ? 0.f : __uint_as_float(w[hd]) * (oscale / l[hd]);
+          const float o = inv[hd] == 0.f ? 0.f : __uint_as_float(w[hd]) * inv[hd];
           const int64_t orow = (int64_t)t * p.h + hd;
           if (p.splits > 1)
             p.o_part[((int64_t)split * p.T * p.h + orow) * p.d_v + ch] = o;
@@ -716,8 +741,7 @@ cudaError_t launch_tc_keys(const FwdParams& p, cudaStream_t stream) {
     const cudaError_t e = encode_bf16_rows_map(&a.kv_map, p.kv, p.d_qk, p.num_slots);
     if (e != cudaSuccess) return e;
   }
-  a.n_chunks[0] = 4;                     // channels [0, 256)
-  a.n_chunks[1] = (p.d_qk - 256) / 64;   // [256, d_qk): 5 (576) or 4 (512)
+  a.ksteps = p.d_qk == 576 ? 18 : 16;
   a.G = (p.d_qk + 127) / 128;
   a.scale_log2 = p.sm_scale * 1.4426950408889634f;
   const int64_t clusters = (int64_t)p.T * p.splits;
