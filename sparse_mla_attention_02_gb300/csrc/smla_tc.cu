@@ -8,9 +8,10 @@
 //   * QK^T is split over d_qk: CTA r keeps Q[:, its half of d_qk] in TMEM
 //     (the MMA's A operand) and computes partial scores S_r = Q_r K_r^T
 //     [128 heads x 48 keys] per block of 48 top-k positions;
-//   * each CTA sends its partial S to the other with st.async (counted on the
-//     receiver's mbarrier), so both hold S = S_0 + S_1 and run the same
-//     softmax for all 128 heads (identical inputs, identical results);
+//   * each CTA sends its partial S to the other with bulk copies (one per
+//     softmax warpgroup, counted on the receiver's mbarrier), so both hold
+//     S = S_0 + S_1 and run the same softmax for all 128 heads (identical
+//     inputs, identical results);
 //   * PV is split over d_v: CTA r accumulates O[:, 256r : 256r+256] in TMEM
 //     from its P [128 x 48] and the first 512 channels of the same gathered
 //     rows (V is the prefix of K).
@@ -33,11 +34,12 @@
 //   a6 PV (tcgen05.mma, A = P from shared memory, B = V tile, MN-major)
 //   a7 epilogue: O / l -> bf16 out (or fp32 partials), LSE = m + ln l
 //
-// Warp roles (288 threads): warp 0 issues MMAs (warp-uniform code, one
+// Warp roles (416 threads): warp 0 issues MMAs (warp-uniform code, one
 // elected lane per batch of MMAs) and owns TMEM; warps 1..3 load the unit's
-// slot ids, then gather with TMA; warps 4..7 (a warpgroup; thread i <-> TMEM lane i <-> head i) run
-// softmax, the exchange, O rescale and the epilogue; warp 8 signals the peer
-// when its partial scores have been consumed.
+// slot ids, then gather with TMA; warps 4..7 and 8..11 are two softmax
+// warpgroups (thread i <-> TMEM lane i <-> head i; positions 0..23 and 24..47
+// of each block), which run the exchange, softmax, O rescale and the
+// epilogue; warp 12 signals the peer when its partial scores were consumed.
 // Every wait is bounded; a wait that runs out records a timeout status, sets
 // an abort flag that skips later waits, and the block finishes normally.
 #include <cuda.h>
@@ -61,11 +63,13 @@ constexpr int kStages = 4;                 // gathered-tile pipeline depth
 constexpr int kAtomBytes = kBN * 128;      // 48 rows x 128 B (64 channels)
 constexpr int kTileBytes = 5 * kAtomBytes; // up to 320 channels per CTA
 constexpr int kPBytes = 128 * 128;         // P: 128 rows x 64 bf16 (48 used)
-// Exchanged partial scores: 128 rows x 48 fp32; the 16-byte chunk c of row i
-// sits at chunk position c ^ (i & 3) (conflict-light row access, no padding).
-constexpr int kXBytes = 128 * kBN * 4;
-constexpr uint32_t kXTxBytes = (uint32_t)kXBytes;  // bytes received per block
-constexpr int kThreads = 288;            // 8 role warps + 1 signal warp
+// Exchanged partial scores: two halves (positions 0..23 and 24..47, one per
+// softmax warpgroup), each 128 rows x 24 fp32 = 96 bytes per row; the 16-byte
+// chunk c of row i sits at position c ^ ((i >> 2) & 1), which keeps a warp's
+// row accesses free of bank conflicts.
+constexpr int kXHalfBytes = 128 * (kBN / 2) * 4;
+constexpr int kXBytes = 2 * kXHalfBytes;
+constexpr int kThreads = 416;            // 12 role warps + 1 signal warp
 constexpr int kProducers = 96;             // warps 1..3 (slot-id prefetch)
 
 // TMEM columns.
@@ -82,7 +86,9 @@ constexpr uint32_t kOffXs = kOffX + 2 * kXBytes;               // send staging
 constexpr int kMaxBlocks = 64;             // covers topk <= 3072 in one range
 constexpr uint32_t kOffSlot = kOffXs + kXBytes;                 // [blocks*48] i32
 constexpr uint32_t kOffMask = kOffSlot + kMaxBlocks * kBN * 4;  // [blocks][2] u32
-constexpr uint32_t kOffBar = (kOffMask + kMaxBlocks * 8 + 7) & ~7u;
+constexpr uint32_t kOffRed = kOffMask + kMaxBlocks * 8;         // [2][2][128] f32 half maxima
+constexpr uint32_t kOffL = kOffRed + 2 * 2 * 128 * 4;            // [2][128] f32 row sums
+constexpr uint32_t kOffBar = (kOffL + 2 * 128 * 4 + 7) & ~7u;
 enum {
   kBarKvFull = 0,
   kBarKvEmpty = kBarKvFull + kStages,
@@ -90,8 +96,8 @@ enum {
   kBarSEmpty = kBarSFull + 2,          // [2]
   kBarPFull = kBarSEmpty + 2,
   kBarPEmpty,
-  kBarXFull,                           // [2]
-  kBarXFree = kBarXFull + 2,           // [2]
+  kBarXFull,                           // [2 buffers][2 halves]
+  kBarXFree = kBarXFull + 4,           // [2]
   kBarXCons = kBarXFree + 2,           // [2]
   kBarODone = kBarXCons + 2,
   kBarOFinal,                          // one phase: the unit's last PV is done
@@ -153,16 +159,17 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarSFull + i), 1);
-      mbar_init(bar(kBarSEmpty + i), 128);
-      mbar_init(bar(kBarXFull + i), 1);
+      mbar_init(bar(kBarSEmpty + i), 256);
+      mbar_init(bar(kBarXFull + 2 * i), 1);
+      mbar_init(bar(kBarXFull + 2 * i + 1), 1);
       mbar_init(bar(kBarXFree + i), 1);
-      mbar_init(bar(kBarXCons + i), 128);
+      mbar_init(bar(kBarXCons + i), 256);
     }
-    mbar_init(bar(kBarPFull), 128);
+    mbar_init(bar(kBarPFull), 256);
     mbar_init(bar(kBarPEmpty), 1);
     mbar_init(bar(kBarODone), 1);
     mbar_init(bar(kBarOFinal), 1);
-    mbar_init(bar(kBarQReady), 128);
+    mbar_init(bar(kBarQReady), 256);
     *abort_flag = 0;
     fence_mbar_init_cluster();
   }
@@ -341,7 +348,7 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
       __syncwarp();
     }
     }
-  } else if (warp == 8) {
+  } else if (warp == 12) {
     // ---- signal warp: tell the peer when its partial scores were consumed --
     // (a release-ordered remote arrival; kept off the softmax warps' path)
     if (lane == 0) {
@@ -351,33 +358,43 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
         mbar_arrive_remote(xfree_peer + 8u * (b & 1));
       }
     }
-  } else {
-    // ---- softmax warpgroup ---------------------------------------------------
-    const int i = tid - 128;                     // head row == TMEM lane
+  } else if (warp <= 11) {
+    // ---- softmax warpgroups --------------------------------------------------
+    // Warpgroup wg (warps 4..7: wg 0, warps 8..11: wg 1) owns positions
+    // [24 wg, 24 wg + 24) of every block; thread i of a warpgroup owns head i
+    // (TMEM lane i).  Each warpgroup exchanges its own half of the partial
+    // scores with the same warpgroup of the peer CTA.  Both warpgroups keep
+    // the same running max m (log2 units): once per block they meet at a
+    // named barrier that also reduces "some half-block max passes m + 8"; only
+    // then do they read each other's half maxima and raise m (identically).
+    const int wg = (warp - 4) >> 2;
+    const int i = (warp & 3) * 32 + lane;        // head row == TMEM lane
     const uint32_t lane_base = ((uint32_t)(warp & 3) * 32u) << 16;
     const int head = i;
-    // Q half -> TMEM (rows >= h are zero).
+    const bool wlead = i == 0;                   // the warpgroup's first thread
+    // Q half -> TMEM (rows >= h are zero): 16-column groups [0, 5) by the
+    // first warpgroup, [5, ksteps / 2) by the second.
     {
-      // All loads of the row are issued before the first TMEM store.
       const uint4* qrow = reinterpret_cast<const uint4*>(
           reinterpret_cast<const uint16_t*>(p.q) +
           ((int64_t)t * p.h + (head < p.h ? head : 0)) * p.d_qk + a.q_lo[r]);
-      const int nchunk = a.ksteps * 2;           // 16-byte chunks: 36 or 32
-      uint4 qv[36];
+      const int g0 = wg == 0 ? 0 : 5, g1 = wg == 0 ? 5 : a.ksteps / 2;
+      uint4 qv[20];
 #pragma unroll
-      for (int c = 0; c < 36; ++c)
-        qv[c] = (head < p.h && c < nchunk) ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
+      for (int c = 0; c < 20; ++c)
+        qv[c] = (head < p.h && c < 4 * (g1 - g0)) ? __ldg(qrow + 4 * g0 + c)
+                                                  : make_uint4(0u, 0u, 0u, 0u);
       __syncwarp();
 #pragma unroll
-      for (int c = 0; c < 9; ++c) {
-        if (4 * c < nchunk) {                    // same for every lane
-          const uint32_t w[16] = {qv[4 * c].x,     qv[4 * c].y,     qv[4 * c].z,
-                                  qv[4 * c].w,     qv[4 * c + 1].x, qv[4 * c + 1].y,
-                                  qv[4 * c + 1].z, qv[4 * c + 1].w, qv[4 * c + 2].x,
-                                  qv[4 * c + 2].y, qv[4 * c + 2].z, qv[4 * c + 2].w,
-                                  qv[4 * c + 3].x, qv[4 * c + 3].y, qv[4 * c + 3].z,
-                                  qv[4 * c + 3].w};
-          tmem_st16(tmem + lane_base + kColQ + 16 * c, w);
+      for (int k = 0; k < 5; ++k) {
+        if (k < g1 - g0) {                       // same for every lane
+          const uint32_t w[16] = {qv[4 * k].x,     qv[4 * k].y,     qv[4 * k].z,
+                                  qv[4 * k].w,     qv[4 * k + 1].x, qv[4 * k + 1].y,
+                                  qv[4 * k + 1].z, qv[4 * k + 1].w, qv[4 * k + 2].x,
+                                  qv[4 * k + 2].y, qv[4 * k + 2].z, qv[4 * k + 2].w,
+                                  qv[4 * k + 3].x, qv[4 * k + 3].y, qv[4 * k + 3].z,
+                                  qv[4 * k + 3].w};
+          tmem_st16(tmem + lane_base + kColQ + 16 * (g0 + k), w);
         }
       }
       tmem_wait_st();
@@ -387,23 +404,26 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
     // E4M3 cache: the per-tensor scale multiplies every score and output.
     const float kscale = a.fp8 ? __ldg(p.k_scale) : 1.f;
     const float scale_log2 = a.scale_log2 * kscale;
-    float m_run = -INFINITY;   // running max (log2 units)
-    float l_run = 0.f;         // running sum of exp2(s - m_run)
-    const float* Xs = reinterpret_cast<const float*>(sm + kOffX);
-    const uint32_t x_peer = mapa(sb + kOffX, peer);
-    const uint32_t xfull_peer = mapa(bar(kBarXFull), peer);
-    const uint32_t xrow = (uint32_t)i * kBN * 4;      // this row's byte offset
-    const uint32_t xsw = (uint32_t)i & 3u;            // its chunk swizzle
+    float m_run = -INFINITY;   // running max (log2 units), same in both warpgroups
+    float l_run = 0.f;         // this warpgroup's running sum of exp2(s - m_run)
+    const uint32_t x_half = (uint32_t)wg * kXHalfBytes;
+    const uint8_t* Xr = sm + kOffX + x_half;           // receive buffers (this half)
+    const uint32_t x_peer = mapa(sb + kOffX + x_half, peer);
+    const uint32_t xfull_peer = mapa(bar(kBarXFull + wg), peer);
+    const uint32_t xrow = (uint32_t)i * (kBN / 2) * 4; // this row's byte offset
+    const uint32_t xsw = ((uint32_t)i >> 2) & 1u;      // its chunk swizzle
+    float* red = reinterpret_cast<float*>(sm + kOffRed);  // [2 buf][2 wg][128]
+    const int nbar = 2 + wg;                           // warpgroup-local barrier
 
-    // O row *= alpha.  tcgen05.ld/st are warp-collective (.sync.aligned), so
-    // the whole warp takes this path when any of its lanes needs it; lanes
-    // with nothing to rescale pass alpha = 1.
+    // O row *= alpha for this warpgroup's 128 columns.  tcgen05.ld/st are
+    // warp-collective (.sync.aligned), so the whole warp takes this path when
+    // any of its lanes needs it; lanes with nothing to rescale pass 1.
     auto rescale_o = [&](float alpha, int b) {
       W.wait(bar(kBarODone), (b - 1) & 1);
       __syncwarp();
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < 256; c += 16) {
+      for (int c = 128 * wg; c < 128 * wg + 128; c += 16) {
         uint32_t w[16];
         tmem_ld16(tmem + lane_base + kColO + c, w);
         tmem_wait_ld();
@@ -413,81 +433,90 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
       }
       tmem_wait_st();
     };
-    // Read this row's partial scores of block j from TMEM, free the S buffer,
-    // stage them in shared memory, and (thread 0) send all 128 rows to the
-    // peer with one bulk copy counted on its X-full barrier for buffer j&1.
-    auto load_and_send = [&](int j, float (&dst)[kBN]) {
+    // Read this half of the row's partial scores of block j from TMEM, free
+    // the S buffer, stage them in shared memory, and (the warpgroup's first
+    // thread) send the 128 rows to the peer with one bulk copy counted on its
+    // X-full barrier for (buffer j & 1, this half).
+    auto load_and_send = [&](int j, float (&dst)[kBN / 2]) {
       const int buf = j & 1;
-      if (i == 0) {
-        mbar_arrive_expect_tx(bar(kBarXFull + buf), kXTxBytes);
+      if (wlead) {
+        mbar_arrive_expect_tx(bar(kBarXFull + 2 * buf + wg), (uint32_t)kXHalfBytes);
         bulk_wait_read_all();                // the previous send has read the stage
       }
       W.wait(bar(kBarSFull + buf), (j >> 1) & 1);
       __syncwarp();
       tc_fence_after();
-      uint32_t w[16];
-#pragma unroll
-      for (int c = 0; c < kBN; c += 16) {
-        tmem_ld16(tmem + lane_base + kColS + kBN * buf + c, w);
+      {
+        uint32_t w16[16], w8[8];
+        const uint32_t col = tmem + lane_base + kColS + kBN * buf + (kBN / 2) * wg;
+        tmem_ld16(col, w16);
+        tmem_ld8(col + 16, w8);
         tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < 16; ++k) dst[c + k] = __uint_as_float(w[k]);
+        for (int k = 0; k < 16; ++k) dst[k] = __uint_as_float(w16[k]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) dst[16 + k] = __uint_as_float(w8[k]);
       }
       tc_fence_before();
       mbar_arrive(bar(kBarSEmpty + buf));
-      named_bar_sync(2, 128);                // staging buffer is free
-      uint8_t* srow = sm + kOffXs + xrow;
+      named_bar_sync(nbar, 128);             // staging half is free
+      uint8_t* srow = sm + kOffXs + x_half + xrow;
 #pragma unroll
-      for (int c = 0; c < kBN / 4; ++c)
+      for (int c = 0; c < kBN / 8; ++c)
         *reinterpret_cast<float4*>(srow + ((((uint32_t)c) ^ xsw) << 4)) =
             make_float4(dst[4 * c], dst[4 * c + 1], dst[4 * c + 2], dst[4 * c + 3]);
       fence_proxy_async_smem();
-      named_bar_sync(2, 128);                // all rows staged
-      if (i == 0) {
+      named_bar_sync(nbar, 128);             // all rows staged
+      if (wlead) {
         if (j >= 2) W.wait(bar(kBarXFree + buf), ((j >> 1) - 1) & 1);
-        bulk_copy_to_peer(x_peer + buf * kXBytes, sb + kOffXs, kXTxBytes, xfull_peer + 8u * buf);
+        bulk_copy_to_peer(x_peer + buf * kXBytes, sb + kOffXs + x_half, (uint32_t)kXHalfBytes,
+                          xfull_peer + 16u * buf);
         bulk_commit_group();
       }
     };
 
-    float sp[kBN], nx[kBN];
+    float sp[kBN / 2], nx[kBN / 2];
     if (nb > 0) load_and_send(0, nx);
     for (int b = 0; b < nb; ++b) {
       const int buf = b & 1;
 #pragma unroll
-      for (int j = 0; j < kBN; ++j) sp[j] = nx[j];
+      for (int j = 0; j < kBN / 2; ++j) sp[j] = nx[j];
       if (b + 1 < nb) load_and_send(b + 1, nx);
-      // The peer's partial for this block; then let the peer reuse the buffer.
-      W.wait_cluster(bar(kBarXFull + buf), (b >> 1) & 1);
-      const uint8_t* xr = reinterpret_cast<const uint8_t*>(Xs) + buf * kXBytes + xrow;
+      // The peer's partial for this half-block; then let the peer reuse it.
+      W.wait_cluster(bar(kBarXFull + 2 * buf + wg), (b >> 1) & 1);
+      const uint8_t* xr = Xr + buf * kXBytes + xrow;
 #pragma unroll
-      for (int c = 0; c < kBN / 4; ++c) {
+      for (int c = 0; c < kBN / 8; ++c) {
         const float4 x = *reinterpret_cast<const float4*>(xr + ((((uint32_t)c) ^ xsw) << 4));
         sp[4 * c] += x.x; sp[4 * c + 1] += x.y; sp[4 * c + 2] += x.z; sp[4 * c + 3] += x.w;
       }
       mbar_arrive(bar(kBarXCons + buf));   // the signal warp tells the peer
       // a5: masked online softmax (log2 domain).
-      const uint32_t m_lo = masks[b * 2], m_hi = masks[b * 2 + 1];
-      float bmax = -INFINITY;
+      const uint64_t vm = ((uint64_t)masks[b * 2 + 1] << 32 | masks[b * 2]) >> (24 * wg);
+      float hm = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < kBN; ++j) {
-        const bool ok = ((j < 32 ? m_lo >> j : m_hi >> (j - 32)) & 1u) != 0u;
-        sp[j] = ok ? sp[j] * scale_log2 : -INFINITY;
-        bmax = fmaxf(bmax, sp[j]);
+      for (int j = 0; j < kBN / 2; ++j) {
+        sp[j] = ((vm >> j) & 1u) ? sp[j] * scale_log2 : -INFINITY;
+        hm = fmaxf(hm, sp[j]);
       }
+      float* rb = red + buf * 256;
+      rb[wg * 128 + i] = hm;
       float alpha = 1.f;
-      if (bmax > m_run + 8.f) {          // also true for the first finite max
-        alpha = ex2_approx(m_run - bmax);  // 0 when m_run = -inf
-        m_run = bmax;
+      if (named_bar_or(4, 256, hm > m_run + 8.f)) {   // also true for the first finite max
+        const float bm = fmaxf(hm, rb[(wg ^ 1) * 128 + i]);
+        if (bm > m_run + 8.f) {
+          alpha = ex2_approx(m_run - bm);             // 0 when m_run = -inf
+          m_run = bm;
+        }
       }
-      uint32_t pk[kBN / 2];
+      uint32_t pk[kBN / 4];
       float lsum = 0.f;
       if (m_run == -INFINITY) {
 #pragma unroll
-        for (int j = 0; j < kBN / 2; ++j) pk[j] = 0u;
+        for (int j = 0; j < kBN / 4; ++j) pk[j] = 0u;
       } else {
 #pragma unroll
-        for (int j = 0; j < kBN; j += 2) {
+        for (int j = 0; j < kBN / 2; j += 2) {
           // The row sum uses the unrounded values (it sets the LSE); P goes
           // to the PV MMA in bf16.
           const float e0 = ex2_approx(sp[j] - m_run), e1 = ex2_approx(sp[j + 1] - m_run);
@@ -497,13 +526,14 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
       }
       l_run = l_run * alpha + lsum;
       if (b >= 1) W.wait(bar(kBarPEmpty), (b - 1) & 1);   // PV(b-1) has read P
-      // P row (48 bf16 = 6 chunks of 16 B) into the 128-byte-swizzled buffer.
+      // This half of the P row (24 bf16 = 3 chunks of 16 B, chunks 3 wg ..
+      // 3 wg + 2) into the 128-byte-swizzled buffer.
       uint8_t* prow = sm + kOffP + i * 128;
 #pragma unroll
-      for (int j = 0; j < kBN / 8; ++j) {
-        const uint32_t off = ((uint32_t)j ^ ((uint32_t)i & 7u)) << 4;
+      for (int c = 0; c < 3; ++c) {
+        const uint32_t off = ((uint32_t)(3 * wg + c) ^ ((uint32_t)i & 7u)) << 4;
         *reinterpret_cast<uint4*>(prow + off) =
-            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       }
       fence_proxy_async_smem();
       if (b >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) rescale_o(alpha, b);
@@ -512,20 +542,27 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
     }
 
     // ---- a7: epilogue ---------------------------------------------------------
-    // (A parity wait on the per-PV barrier could pass a phase early when two
-    // PVs are still in flight; the final barrier has exactly one phase.)
+    // l = the two warpgroups' sums.  (A parity wait on the per-PV barrier
+    // could pass a phase early when two PVs are still in flight; the final
+    // barrier has exactly one phase.)
+    float* lsh = reinterpret_cast<float*>(sm + kOffL);  // [2][128]
+    lsh[wg * 128 + i] = l_run;
+    named_bar_sync(4, 256);
+    const float l_tot = lsh[i] + lsh[128 + i];
     if (nb > 0) {
       W.wait(bar(kBarOFinal), 0);
+      __syncwarp();
       tc_fence_after();
     }
-    const bool empty = !(l_run > 0.f) || nb == 0;
-    const float inv = empty ? 0.f : kscale / l_run;
+    const bool empty = !(l_tot > 0.f) || nb == 0;
+    const float inv = empty ? 0.f : kscale / l_tot;
     const bool live = head < p.h;          // pad rows past h are not written
     const int64_t orow = (int64_t)t * p.h + (live ? head : 0);
     // Every lane of the warpgroup runs the TMEM loads (warp-collective);
-    // only the stores depend on the lane's head.
+    // only the stores depend on the lane's head.  Warpgroup wg writes output
+    // channels [256 r + 128 wg, 256 r + 128 wg + 128).
 #pragma unroll 1
-    for (int c = 0; c < 256; c += 16) {
+    for (int c = 128 * wg; c < 128 * wg + 128; c += 16) {
       uint32_t w[16];
       __syncwarp();
       if (nb > 0) {
@@ -555,10 +592,11 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
         *reinterpret_cast<uint4*>(dst + 8) = make_uint4(o[4], o[5], o[6], o[7]);
       }
     }
-    // Both CTAs hold the same LSE; CTA r writes heads [64r, 64r + 64).
-    if (live && (uint32_t)(i >> 6) == r) {
+    // Both CTAs hold the same LSE; the first warpgroup of CTA r writes heads
+    // [64r, 64r + 64).
+    if (wg == 0 && live && (uint32_t)(i >> 6) == r) {
       const float lse_v =
-          empty ? -INFINITY : (m_run + log2f(l_run)) * 0.69314718055994530942f;
+          empty ? -INFINITY : (m_run + log2f(l_tot)) * 0.69314718055994530942f;
       if (p.splits > 1)
         p.lse_part[(int64_t)split * p.T * p.h + orow] = lse_v;
       else if (p.lse)
@@ -567,10 +605,11 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
   }
 
   // ---- teardown: no CTA leaves while its peer may still write into it -----
-  // The peer's last X-free arrivals land asynchronously: wait for the final
-  // phases of both X-free barriers first.
+  // Each warpgroup's sends have read their stage; the peer's last X-free
+  // arrivals land asynchronously: wait for the final phases of both X-free
+  // barriers first.
+  if ((tid == 128 || tid == 256) && nb > 0) bulk_wait_read_all();
   if (tid == 128 && nb > 0) {
-    bulk_wait_read_all();
     if (nb >= 2) W.wait(bar(kBarXFree + ((nb - 2) & 1)), ((nb - 2) >> 1) & 1);
     W.wait(bar(kBarXFree + ((nb - 1) & 1)), ((nb - 1) >> 1) & 1);
   }

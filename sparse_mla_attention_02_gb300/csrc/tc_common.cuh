@@ -13,12 +13,18 @@
 
 namespace smla {
 
+// Named barriers over whole warps.  bar.sync / bar.red are the .aligned
+// forms: every lane of a warp must execute them together, so the warp is
+// reconverged first (lanes leave a spin-wait loop at different times, and an
+// aligned barrier reached by a split warp is undefined behaviour).
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
+  __syncwarp();
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
 // OR of `pred` over the `n` threads that meet at named barrier `id`.
 __device__ __forceinline__ bool named_bar_or(int id, int n, bool pred) {
+  __syncwarp();
   uint32_t out;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
