@@ -348,7 +348,8 @@ def run_ours(args, rank, world, local_rank):
                 "roofline_frac": round(max(fl2 / (pk["bf16_tflops"] * 1e12),
                                            U2 / (pk["hbm_gbs"] * 1e9)) / t2, 4),
                 "splits_workspace_bytes": n2,
-                "kernel": "tcgen05" if w2.kv_dtype != W.KV_FP8_E4M3_GROUP128 else "cuda-core",
+                "kernel": smla.smla_plan_info(w2.T, w2.h, w2.d_qk, w2.topk,
+                                              w2.kv_dtype)["kernel"],
             }
             del w2, ws2, out2, lse2
             torch.cuda.empty_cache()

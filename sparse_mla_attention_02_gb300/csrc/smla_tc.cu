@@ -194,14 +194,8 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
     const int pt = tid - 32;
     const int32_t* idx_row = p.indices + (int64_t)t * p.topk;
     const int n = nb * kBN;
-    bool bad = false;
-    for (int jj = pt; jj < n; jj += kProducers) {
-      const int pos = k0 + jj;
-      int id = pos < k1 ? __ldg(idx_row + pos) : -1;
-      if (id >= p.num_slots) { bad = true; id = -1; }
-      slots[jj] = id < 0 ? -1 : id;
-    }
-    if (bad) atomicCAS(p.status, 0, kStatusBadIndex);
+    if (load_slot_ids(idx_row, k0, k1, p.topk, n, p.num_slots, slots, pt, kProducers))
+      atomicCAS(p.status, 0, kStatusBadIndex);
     named_bar_sync(1, kProducers);
     if (warp < 3) {                        // warp 1: rows 0..31, warp 2: rows 32..47
       const int row = (warp - 1) * 32 + lane;

@@ -238,14 +238,8 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
     const int pt = tid - 32;
     const int32_t* idx_row = p.indices + (int64_t)t * p.topk;
     const int n = nb * kBK;
-    bool bad = false;
-    for (int jj = pt; jj < n; jj += kProducers) {
-      const int pos = k0 + jj;
-      int id = pos < k1 ? __ldg(idx_row + pos) : -1;
-      if (id >= p.num_slots) { bad = true; id = -1; }
-      slots[jj] = id < 0 ? -1 : id;
-    }
-    if (bad) atomicCAS(p.status, 0, kStatusBadIndex);
+    if (load_slot_ids(idx_row, k0, k1, p.topk, n, p.num_slots, slots, pt, kProducers))
+      atomicCAS(p.status, 0, kStatusBadIndex);
     named_bar_sync(1, kProducers);
     const int row = (warp - 1) * 32 + lane;
     for (int b = 0; b < nb; ++b) {
@@ -357,6 +351,18 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
         for (int u = 0; u < 18; ++u)
           rw[u] = (id >= 0 && u < n_u) ? __ldg(u < 16 ? src + u : srope + (u - 16))
                                        : make_uint4(0u, 0u, 0u, 0u);
+        if (b + 1 < nb) {
+          // the row of the next block into L2 while this one is converted
+          const int idn = slots[(b + 1) * kBK + row];
+          if (idn >= 0) {
+            const uint8_t* rn = kv8 + (size_t)idn * p.d_qk;
+            prefetch_l2(rn + g_lo);
+            prefetch_l2(rn + g_lo + 128);
+            prefetch_l2(rn + g_lo + 255);
+            if (n_u > 16) prefetch_l2(rn + rope_lo);
+            if (kGroup) prefetch_l2(p.k_scale + (int64_t)idn * a.G);
+          }
+        }
         float sc[3] = {0.f, 0.f, 0.f};
         if (kGroup && id >= 0) {
           const float* srow = p.k_scale + (int64_t)id * a.G;

@@ -196,6 +196,11 @@ __device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, u
       : "memory");
 }
 
+// Hint: bring the cache line holding src into L2 without waiting for it.
+__device__ __forceinline__ void prefetch_l2(const void* src) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(src) : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
