@@ -151,6 +151,48 @@ SMLA_API smla_status smla_fwd_ws(const void* q, const void* kv_cache, int kv_dty
                         size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * smla_fwd_paged — smla_fwd for request-local top-k indices, translated to
+ * cache slots inside the kernels' index loads (the fused form of the index
+ * conversion the serving backends run as a separate kernel before the
+ * attention call: vLLM "Sparse MLA on Hopper" diff, the kernel test file's
+ * index-conversion tests (2.5, 2.9), which fix
+ *   slot = block_table[req, e / block_size] * block_size + e % block_size
+ * with -1 entries propagated).
+ *  token_indices      device int32 [T, topk]: positions in the token's
+ *                     request (its KV sequence); entries < 0 are masked.
+ *  req_id_per_token   device int32 [T]: the token's request, in [0, num_reqs);
+ *                     a token outside that range has every entry masked and
+ *                     sets the SMLA_ERR_BAD_INDEX device status.
+ *  block_table        device int32 [num_reqs, block_table_stride]: the cache
+ *                     block of each block_size positions of a request; a
+ *                     negative entry is an unallocated block (its positions
+ *                     are masked).  A position whose block index is
+ *                     >= block_table_stride, or whose slot is >= num_slots,
+ *                     is masked and sets SMLA_ERR_BAD_INDEX.
+ *  block_size         positions per block (>= 1).
+ *  block_stride_rows  cache rows between consecutive blocks: slot =
+ *                     block * block_stride_rows + e % block_size; 0 means
+ *                     block_size (the pages' BLOCK_STRIDE_ROWS option).
+ *  workspace          caller-owned workspace as for smla_fwd_ws, or NULL to
+ *                     use the library-owned one as smla_fwd does.
+ * Every other argument, the result and the errors are those of smla_fwd:
+ * the call computes exactly what smla_fwd computes on the translated slot
+ * ids (the same kernels read the same rows).  Host checks add:
+ * SMLA_ERR_INVALID_ARG when block_table or req_id_per_token is NULL or
+ * unaligned, or num_reqs, block_table_stride or block_size < 1.
+ */
+SMLA_API smla_status smla_fwd_paged(const void* q, const void* kv_cache, int kv_dtype,
+                           const float* k_scale, const int32_t* token_indices,
+                           const int32_t* req_id_per_token,
+                           const int32_t* block_table, int num_reqs,
+                           int block_table_stride, int block_size,
+                           int block_stride_rows, const int32_t* valid_len,
+                           int T, int h, int d_qk, int d_v, int topk,
+                           int64_t num_slots, float sm_scale, void* out,
+                           float* lse, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+
+/*
  * smla_combine — LSE-weighted merge of partial results computed over disjoint
  * key sets (the split-KV combine, and the cross-rank merge of the
  * flashmla_sparse page's DCP path):

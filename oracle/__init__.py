@@ -142,3 +142,43 @@ def merge(o_parts, lse_parts):
     lib.smla_oracle_merge(_ptr(o_parts), _ptr(lse_parts), P, rows, d_v,
                           _ptr(out), _ptr(lse))
     return out, lse
+
+
+def paged_to_global(token_indices, req_id, block_table, block_size,
+                    block_stride_rows=0):
+    """Request-local top-k positions -> global cache slots, entry by entry.
+
+    Follows the index conversion the serving backends run before the
+    attention call (vLLM "Sparse MLA on Hopper" diff, kernel test file,
+    index-conversion tests 2.5 and 2.9): for a position e >= 0 of token t in
+    request r = req_id[t],
+        slot = block_table[r, e // block_size] * stride + e % block_size,
+    stride = block_stride_rows or block_size (the BLOCK_STRIDE_ROWS option);
+    entries < 0 stay -1.  Readings where the pages are silent: a request id
+    outside [0, num_reqs), a block index past the table's width, and a
+    negative (unallocated) table entry all give -1.  Returns int64 [T, topk]
+    with -1 for masked entries; slots past the cache are left for the
+    forward to mask.
+    """
+    idx = np.asarray(token_indices, dtype=np.int64)
+    req = np.asarray(req_id, dtype=np.int64)
+    table = np.asarray(block_table, dtype=np.int64)
+    stride = int(block_stride_rows) or int(block_size)
+    T, K = idx.shape
+    out = np.full((T, K), -1, dtype=np.int64)
+    for t in range(T):
+        r = int(req[t])
+        if r < 0 or r >= table.shape[0]:
+            continue
+        for j in range(K):
+            e = int(idx[t, j])
+            if e < 0:
+                continue
+            page = e // block_size
+            if page >= table.shape[1]:
+                continue
+            blk = int(table[r, page])
+            if blk < 0:
+                continue
+            out[t, j] = blk * stride + e % block_size
+    return out

@@ -58,6 +58,9 @@ def load():
         lib.smla_fwd.restype = I
         lib.smla_fwd_ws.argtypes = fwd_args + [P, SZ, P]
         lib.smla_fwd_ws.restype = I
+        lib.smla_fwd_paged.argtypes = [P, P, I, P, P, P, P, I, I, I, I, P, I, I, I,
+                                       I, I, I64, F, P, P, P, SZ, P]
+        lib.smla_fwd_paged.restype = I
         lib.smla_workspace_size.argtypes = [I, I, I, I, I, I]
         lib.smla_workspace_size.restype = SZ
         lib.smla_plan_info.argtypes = [I, I, I, I, I, I, ctypes.POINTER(I),
@@ -138,6 +141,37 @@ def smla_fwd(q, kv_cache, kv_dtype, k_scale, indices, valid_len, sm_scale,
     args, out, lse = _fwd_args(q, kv_cache, kv_dtype, k_scale, indices,
                                valid_len, sm_scale, out, lse, num_slots)
     _check(lib.smla_fwd(*args, _stream(stream)), "smla_fwd")
+    return out, lse
+
+
+def smla_fwd_paged(q, kv_cache, kv_dtype, k_scale, token_indices, req_id,
+                   block_table, block_size, sm_scale, valid_len=None,
+                   block_stride_rows=0, out=None, lse=None, want_lse=True,
+                   num_slots=None, workspace=None, stream=None):
+    """``smla_fwd_paged``: the forward on request-local top-k indices.
+
+    token_indices int32 [T,topk] (positions in the token's request, -1 =
+    none); req_id int32 [T]; block_table int32 [num_reqs, stride]; the slot
+    of position e is block_table[req, e // block_size] * block_stride_rows +
+    e % block_size (block_stride_rows 0 = block_size).  workspace: a uint8
+    device tensor (caller-owned, as smla_fwd_ws) or None (library-owned).
+    Returns (out, lse) as smla_fwd."""
+    import torch
+    lib = load()
+    if lse is None and want_lse:
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    args, out, lse = _fwd_args(q, kv_cache, kv_dtype, k_scale, token_indices,
+                               valid_len, sm_scale, out, lse, num_slots)
+    for x in (req_id, block_table):
+        assert x.is_cuda and x.dtype == torch.int32 and x.is_contiguous()
+    assert req_id.shape == (args[6],) and block_table.dim() == 2
+    ws_p = None if workspace is None else _p(workspace)
+    ws_n = 0 if workspace is None else workspace.numel()
+    pargs = args[:4] + [args[4], _p(req_id), _p(block_table),
+                        int(block_table.shape[0]), int(block_table.shape[1]),
+                        int(block_size), int(block_stride_rows), args[5]] + args[6:]
+    _check(lib.smla_fwd_paged(*pargs, ws_p, ws_n, _stream(stream)),
+           "smla_fwd_paged")
     return out, lse
 
 

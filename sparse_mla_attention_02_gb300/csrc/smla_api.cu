@@ -76,15 +76,29 @@ smla_status check_args(const void* q, const void* kv, int kv_dtype,
   return SMLA_OK;
 }
 
+// Request-local index translation (smla_fwd_paged); table == nullptr for
+// global slot ids.
+struct Paged {
+  const int32_t* req_id = nullptr;
+  const int32_t* table = nullptr;
+  int num_reqs = 0, bt_stride = 0, block_size = 0, stride_rows = 0;
+};
+
 smla_status run_fwd(const void* q, const void* kv, int kv_dtype,
                     const float* k_scale, const int32_t* indices,
                     const int32_t* valid_len, int T, int h, int d_qk, int d_v,
                     int topk, int64_t num_slots, float sm_scale, void* out,
                     float* lse, void* ws, size_t ws_bytes, bool own_ws,
-                    cudaStream_t stream) {
+                    cudaStream_t stream, const Paged& pg = Paged()) {
   smla_status st = check_args(q, kv, kv_dtype, k_scale, indices, T, h, d_qk,
                               d_v, topk, num_slots, out);
   if (st != SMLA_OK || T == 0) return st;
+  if (pg.table) {
+    if (!pg.req_id || pg.num_reqs < 1 || pg.bt_stride < 1 || pg.block_size < 1 ||
+        pg.stride_rows < 1 || !aligned(pg.req_id, 4) || !aligned(pg.table, 4) ||
+        (int64_t)pg.num_reqs * pg.bt_stride > 0x7FFFFFFFLL)
+      return SMLA_ERR_INVALID_ARG;
+  }
   if ((valid_len && !aligned(valid_len, 4)) || (lse && !aligned(lse, 4)))
     return SMLA_ERR_INVALID_ARG;
   DeviceInfo* dev = nullptr;
@@ -130,6 +144,12 @@ smla_status run_fwd(const void* q, const void* kv, int kv_dtype,
   p.splits = plan.splits;
   p.split_len = plan.split_len;
   p.sm_scale = sm_scale;
+  p.req_id = pg.req_id;
+  p.block_table = pg.table;
+  p.num_reqs = pg.num_reqs;
+  p.bt_stride = pg.bt_stride;
+  p.block_size = pg.block_size;
+  p.block_stride_rows = pg.stride_rows;
   if (plan.splits > 1) {
     p.o_part = static_cast<float*>(ws);
     p.lse_part = p.o_part + (size_t)plan.splits * T * h * d_v;
@@ -225,6 +245,29 @@ smla_status smla_fwd_ws(const void* q, const void* kv_cache, int kv_dtype,
   return run_fwd(q, kv_cache, kv_dtype, k_scale, indices, valid_len, T, h,
                  d_qk, d_v, topk, num_slots, sm_scale, out, lse, workspace,
                  workspace_bytes, false, stream);
+}
+
+smla_status smla_fwd_paged(const void* q, const void* kv_cache, int kv_dtype,
+                           const float* k_scale, const int32_t* token_indices,
+                           const int32_t* req_id_per_token,
+                           const int32_t* block_table, int num_reqs,
+                           int block_table_stride, int block_size,
+                           int block_stride_rows, const int32_t* valid_len,
+                           int T, int h, int d_qk, int d_v, int topk,
+                           int64_t num_slots, float sm_scale, void* out,
+                           float* lse, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream) {
+  if (!block_table) return SMLA_ERR_INVALID_ARG;
+  Paged pg;
+  pg.req_id = req_id_per_token;
+  pg.table = block_table;
+  pg.num_reqs = num_reqs;
+  pg.bt_stride = block_table_stride;
+  pg.block_size = block_size;
+  pg.stride_rows = block_stride_rows == 0 ? block_size : block_stride_rows;
+  return run_fwd(q, kv_cache, kv_dtype, k_scale, token_indices, valid_len, T, h,
+                 d_qk, d_v, topk, num_slots, sm_scale, out, lse, workspace,
+                 workspace_bytes, workspace == nullptr, stream, pg);
 }
 
 size_t smla_workspace_size(int T, int h, int d_qk, int d_v, int topk,

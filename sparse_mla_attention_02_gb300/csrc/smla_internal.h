@@ -32,7 +32,51 @@ struct FwdParams {
   int splits;             // top-k position ranges per (token, head group)
   int split_len;          // positions per range
   float sm_scale;
+  // Request-local indices (block_table != nullptr): indices hold positions
+  // in the token's request; slot = block_table[req, pos / block_size] *
+  // block_stride_rows + pos % block_size (see smla_fwd_paged).
+  const int32_t* req_id;       // [T]
+  const int32_t* block_table;  // [num_reqs, bt_stride]
+  int num_reqs, bt_stride, block_size, block_stride_rows;
 };
+
+#ifdef __CUDACC__
+// The global slot for top-k entry value `e` of a token whose request is
+// `req` (-1 when the token's request id is out of range): e itself for
+// global indices; the block-table translation for request-local ones.
+// -1 when masked (e < 0, a page past the table or an unallocated page, or a
+// slot >= num_slots); the out-of-range cases set *bad.
+__device__ __forceinline__ int to_slot(const FwdParams& p, int req, int e, bool& bad) {
+  int64_t id = e;
+  if (p.block_table && e >= 0) {
+    const int page = e / p.block_size;
+    if (req < 0 || page >= p.bt_stride) {
+      bad = true;
+      return -1;
+    }
+    const int blk = __ldg(p.block_table + (int64_t)req * p.bt_stride + page);
+    if (blk < 0) return -1;
+    id = (int64_t)blk * p.block_stride_rows + (e - page * p.block_size);
+  }
+  if (id >= p.num_slots) {
+    bad = true;
+    return -1;
+  }
+  return id < 0 ? -1 : (int)id;
+}
+
+// The request of token t for to_slot (0 for global indices; -1 when out of
+// range, which masks the token's whole row and sets *bad).
+__device__ __forceinline__ int token_req(const FwdParams& p, int t, bool& bad) {
+  if (!p.block_table) return 0;
+  const int req = __ldg(p.req_id + t);
+  if (req < 0 || req >= p.num_reqs) {
+    bad = true;
+    return -1;
+  }
+  return req;
+}
+#endif
 
 // Which kernel family a plan uses.
 enum KernelKind { kKernelSimt = 0, kKernelTc = 1, kKernelTcKeys = 2 };

@@ -105,13 +105,12 @@ smla_simt_kernel(FwdParams p, int n_groups) {
     if (tid < kBlock) {
       int j = kb + tid, id = -1;
       if (j < k1) {
-        id = p.indices[(int64_t)t * p.topk + j];
-        if (id >= p.num_slots) {
-          atomicCAS(p.status, 0, kStatusBadIndex);
-          id = -1;
-        }
+        bool bad = false;
+        const int req = token_req(p, t, bad);
+        id = to_slot(p, req, p.indices[(int64_t)t * p.topk + j], bad);
+        if (bad) atomicCAS(p.status, 0, kStatusBadIndex);
       }
-      slot[tid] = id < 0 ? -1 : id;
+      slot[tid] = id;
     }
     __syncthreads();
     // a2 + a3: gather (and dequantize) the rows; masked rows are zero.

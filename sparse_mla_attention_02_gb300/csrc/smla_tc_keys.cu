@@ -236,9 +236,8 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
   uint32_t* masks = reinterpret_cast<uint32_t*>(sm + kOffMask);
   if (warp >= 1 && warp <= 4) {
     const int pt = tid - 32;
-    const int32_t* idx_row = p.indices + (int64_t)t * p.topk;
     const int n = nb * kBK;
-    if (load_slot_ids(idx_row, k0, k1, p.topk, n, p.num_slots, slots, pt, kProducers))
+    if (load_slot_ids(p, t, k0, k1, n, slots, pt, kProducers))
       atomicCAS(p.status, 0, kStatusBadIndex);
     named_bar_sync(1, kProducers);
     const int row = (warp - 1) * 32 + lane;

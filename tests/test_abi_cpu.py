@@ -103,3 +103,32 @@ def test_plan_info_argument_checks(lib):
     assert q(4, 16, 576, 256, 64, 0) == 2
     assert q(4, 16, 576, 512, 64, 3) == 2
     assert k.value == -1                      # outputs untouched on error
+
+
+def _fwd_paged(lib, **kw):
+    a = dict(q=1 << 12, kv=1 << 12, kv_dtype=0, k_scale=None, idx=1 << 12,
+             req=1 << 12, bt=1 << 12, nreq=2, bts=8, bs=64, bsr=0,
+             valid=None, T=4, h=16, d_qk=576, d_v=512, topk=64, S=256,
+             scale=0.04, out=1 << 12, lse=None)
+    a.update(kw)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.smla_fwd_paged(
+        P(a["q"]), P(a["kv"]), a["kv_dtype"], P(a["k_scale"]), P(a["idx"]),
+        P(a["req"]), P(a["bt"]), a["nreq"], a["bts"], a["bs"], a["bsr"],
+        P(a["valid"]), a["T"], a["h"], a["d_qk"], a["d_v"], a["topk"], a["S"],
+        a["scale"], P(a["out"]), P(a["lse"]), None, 0, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bt=None), 1), (dict(req=None), 1), (dict(nreq=0), 1),
+    (dict(bts=0), 1), (dict(bs=0), 1), (dict(bsr=-1), 1),
+    (dict(req=(1 << 12) + 2), 1), (dict(bt=(1 << 12) + 1), 1),
+    (dict(nreq=1 << 20, bts=1 << 12), 1),
+    (dict(h=0), 1), (dict(idx=None), 1), (dict(d_qk=128), 2),
+])
+def test_paged_bad_arguments_are_rejected_on_the_host(lib, kw, code):
+    assert _fwd_paged(lib, **kw) == code
+
+
+def test_paged_zero_tokens_is_ok(lib):
+    assert _fwd_paged(lib, T=0, q=None, kv=None, idx=None, out=None) == 0

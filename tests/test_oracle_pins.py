@@ -325,3 +325,56 @@ def test_config_inputs_have_the_stated_structure():
         row = p.indices[t].numpy()
         assert np.all(row[:v] <= t) and len(set(row[:v])) == v
         assert np.all(row[v:] == -1)
+
+
+# ---- request-local index conversion (paged_to_global) ----------------------
+# Pinned against the pages' worked cases and an independent construction, not
+# against a retyping of the formula.
+
+
+def test_paged_identity_table_gives_positions():
+    """Kernel test file, test 2.9: with block_table = arange(num_blocks) and
+    positions 0..nv-1 the converted ids equal the positions; -1 tails stay
+    -1 and the valid counts (non -1 entries, test 2.5) are [1, 10, 50, 100]."""
+    T, topk, nblk, bs = 4, 128, 16, 64
+    valid = [1, 10, 50, 100]
+    idx = np.full((T, topk), -1, dtype=np.int64)
+    for t, nv in enumerate(valid):
+        idx[t, :nv] = np.arange(nv)
+    out = oracle.paged_to_global(idx, np.zeros(T), np.arange(nblk)[None, :], bs)
+    for t, nv in enumerate(valid):
+        assert np.array_equal(out[t, :nv], np.arange(nv))
+        assert np.all(out[t, nv:] == -1)
+        assert int((out[t] >= 0).sum()) == nv
+
+
+def test_paged_inverts_a_random_block_assignment():
+    """Build the global slots first (block b, offset o), place each block at
+    a random page of a random request, derive the request-local position
+    page * bs + o, and check the conversion recovers b * stride + o."""
+    rng = np.random.default_rng(5)
+    R, pages, bs, stride = 3, 6, 16, 24
+    nblocks = R * pages
+    perm = rng.permutation(nblocks).reshape(R, pages)   # table[r, page] = block
+    T, K = 7, 20
+    req = rng.integers(0, R, size=T)
+    page = rng.integers(0, pages, size=(T, K))
+    off = rng.integers(0, bs, size=(T, K))
+    blk = perm[req[:, None], page]
+    local = page * bs + off
+    local[:, -3:] = -1
+    out = oracle.paged_to_global(local, req, perm, bs, block_stride_rows=stride)
+    want = blk * stride + off
+    want[:, -3:] = -1
+    assert np.array_equal(out, want)
+
+
+def test_paged_masks_what_cannot_be_translated():
+    """Readings: a page past the table, an unallocated (-1) block and a
+    request id outside the table all give -1."""
+    table = np.array([[4, -1, 7]])
+    idx = np.array([[0, 5, 15, 16, 40, 47, 48, 100]])
+    out = oracle.paged_to_global(idx, [0], table, 16)
+    assert out.tolist() == [[64, 69, 79, -1, 120, 127, -1, -1]]
+    assert oracle.paged_to_global(idx, [1], table, 16).tolist() == [[-1] * 8]
+    assert oracle.paged_to_global(idx, [-1], table, 16).tolist() == [[-1] * 8]
