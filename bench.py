@@ -351,6 +351,40 @@ def run_ours(args, rank, world, local_rank):
                 "kernel": smla.smla_plan_info(w2.T, w2.h, w2.d_qk, w2.topk,
                                               w2.kv_dtype)["kernel"],
             }
+            if name == "bf16_decode":
+                # The same decode step on request-local positions through
+                # smla_fwd_paged: request r's 32768-slot context as 512
+                # blocks of 64 (block_table[r, page] = 512 r + page); the
+                # translation runs inside the kernel's slot-id load.
+                per_req, bs = w2.num_slots // w2.T, 64
+                req = torch.arange(w2.T, dtype=torch.int32, device=dev)
+                table = (torch.arange(w2.T, device=dev)[:, None] * (per_req // bs) +
+                         torch.arange(per_req // bs, device=dev)[None, :]).int().contiguous()
+                local = torch.where(w2.indices >= 0,
+                                    w2.indices - req[:, None] * per_req,
+                                    w2.indices).int().contiguous()
+
+                def f3():
+                    smla.smla_fwd_paged(w2.q, w2.kv, w2.kv_dtype, w2.k_scale, local,
+                                        req, table, bs, w2.sm_scale,
+                                        valid_len=w2.valid_len, out=out2, lse=lse2,
+                                        num_slots=w2.num_slots,
+                                        workspace=ws2 if n2 > 0 else None,
+                                        stream=stream)
+                with torch.cuda.stream(stream):
+                    for _ in range(args.warmup):
+                        f3()
+                stream.synchronize()
+                barrier()
+                el3 = ranks_max(time_steps(f3, k2, stream))
+                t3 = el3 / k2
+                secondary["bf16_decode_paged"] = {
+                    "tflops": round(world * fl2 / t3 / 1e12, 3),
+                    "tokens_per_s": round(world * w2.T / t3, 1),
+                    "ms_per_step": round(1e3 * t3, 4),
+                    "vs_global_indices": round(t2 / t3, 4),
+                    "kernel": "as bf16_decode, request-local indices + block table",
+                }
             del w2, ws2, out2, lse2
             torch.cuda.empty_cache()
 

@@ -193,7 +193,7 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
   if (warp >= 1 && warp < 4) {
     const int pt = tid - 32;
     const int n = nb * kBN;
-    if (load_slot_ids(p, t, k0, k1, n, slots, pt, kProducers))
+    if (load_unit_slots(p, t, k0, k1, n, slots, pt, kProducers))
       atomicCAS(p.status, 0, kStatusBadIndex);
     named_bar_sync(1, kProducers);
     if (warp < 3) {                        // warp 1: rows 0..31, warp 2: rows 32..47

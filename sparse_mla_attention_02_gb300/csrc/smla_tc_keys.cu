@@ -237,7 +237,7 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
   if (warp >= 1 && warp <= 4) {
     const int pt = tid - 32;
     const int n = nb * kBK;
-    if (load_slot_ids(p, t, k0, k1, n, slots, pt, kProducers))
+    if (load_unit_slots(p, t, k0, k1, n, slots, pt, kProducers))
       atomicCAS(p.status, 0, kStatusBadIndex);
     named_bar_sync(1, kProducers);
     const int row = (warp - 1) * 32 + lane;

@@ -85,20 +85,17 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// The slot ids at top-k positions [k0, k0 + n) of token t's index row into
-// slots[0, n) (n a multiple of 4), -1 where masked: at or past k1, or as
-// to_slot decides (negative, translated through the block table for
-// request-local indices, >= num_slots; out-of-range cases make the return
-// value true).  The nthr threads (index pt) share the row in 4-id pieces;
-// each thread issues every load of a batch of 8 pieces before its first
-// store (16-byte loads when the row position is 16-byte aligned), so a
-// unit's ids arrive in about one memory latency (two with a block table)
-// instead of one latency per id.
-__device__ __forceinline__ bool load_slot_ids(const FwdParams& p, int t, int k0, int k1, int n,
-                                              int* slots, int pt, int nthr) {
+// The slot ids at top-k positions [k0, k0 + n) of one index row into
+// slots[0, n) (n a multiple of 4), -1 where masked: at or past k1, negative,
+// or >= num_slots (the last makes the return value true).  The nthr threads
+// (index pt) share the row in 4-id pieces; each thread issues every load of
+// a batch of 8 pieces before its first store (16-byte loads when the row
+// position is 16-byte aligned), so a unit's ids arrive in about one memory
+// latency instead of one latency per id.
+__device__ __forceinline__ bool load_slot_ids(const int32_t* row, int k0, int k1, int topk,
+                                              int n, int64_t num_slots, int* slots, int pt,
+                                              int nthr) {
   bool bad = false;
-  const int32_t* row = p.indices + (int64_t)t * p.topk;
-  const int req = token_req(p, t, bad);
   const bool vec = (reinterpret_cast<uintptr_t>(row + k0) & 15u) == 0;
   for (int base = 4 * pt; base < n; base += 4 * nthr * 8) {
     int4 v[8];
@@ -108,13 +105,13 @@ __device__ __forceinline__ bool load_slot_ids(const FwdParams& p, int t, int k0,
       const int pos = k0 + j;
       v[u] = make_int4(-1, -1, -1, -1);
       if (j < n && pos < k1) {
-        if (vec && pos + 3 < p.topk) {
+        if (vec && pos + 3 < topk) {
           v[u] = __ldg(reinterpret_cast<const int4*>(row + pos));
         } else {
           v[u].x = __ldg(row + pos);
-          if (pos + 1 < p.topk) v[u].y = __ldg(row + pos + 1);
-          if (pos + 2 < p.topk) v[u].z = __ldg(row + pos + 2);
-          if (pos + 3 < p.topk) v[u].w = __ldg(row + pos + 3);
+          if (pos + 1 < topk) v[u].y = __ldg(row + pos + 1);
+          if (pos + 2 < topk) v[u].z = __ldg(row + pos + 2);
+          if (pos + 3 < topk) v[u].w = __ldg(row + pos + 3);
         }
       }
     }
@@ -124,12 +121,58 @@ __device__ __forceinline__ bool load_slot_ids(const FwdParams& p, int t, int k0,
       if (j < n) {
         const int e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          slots[j + q] = k0 + j + q < k1 ? to_slot(p, req, e[q], bad) : -1;
+        for (int q = 0; q < 4; ++q) {
+          int id = k0 + j + q < k1 ? e[q] : -1;
+          if (id >= num_slots) {
+            bad = true;
+            id = -1;
+          }
+          slots[j + q] = id < 0 ? -1 : id;
+        }
       }
     }
   }
   return bad;
+}
+
+// The same for request-local positions (smla_fwd_paged): each loaded entry
+// is translated through the block table by to_slot.  The row's table
+// lookups of a batch are issued together as well (two memory latencies per
+// batch).
+__device__ __forceinline__ bool load_slot_ids_paged(const FwdParams& p, int t, int k0, int k1,
+                                                    int n, int* slots, int pt, int nthr) {
+  bool bad = false;
+  const int32_t* row = p.indices + (int64_t)t * p.topk;
+  const int req = token_req(p, t, bad);
+  for (int base = 4 * pt; base < n; base += 4 * nthr * 8) {
+    int e[8][4];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = base + 4 * nthr * u;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int pos = k0 + j + q;
+        e[u][q] = (j < n && pos < k1) ? __ldg(row + pos) : -1;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = base + 4 * nthr * u;
+      if (j < n) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) slots[j + q] = to_slot(p, req, e[u][q], bad);
+      }
+    }
+  }
+  return bad;
+}
+
+// Either loader, by the launch's index kind.
+__device__ __forceinline__ bool load_unit_slots(const FwdParams& p, int t, int k0, int k1, int n,
+                                                int* slots, int pt, int nthr) {
+  if (p.block_table) return load_slot_ids_paged(p, t, k0, k1, n, slots, pt, nthr);
+  return load_slot_ids(p.indices + (int64_t)t * p.topk, k0, k1, p.topk, n, p.num_slots, slots,
+                       pt, nthr);
 }
 
 // A bf16 cache [num_slots, d_qk] as a 2-D tensor with 64-channel x 1-row
