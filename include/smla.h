@@ -151,6 +151,28 @@ SMLA_API smla_status smla_fwd_ws(const void* q, const void* kv_cache, int kv_dty
                         size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * smla_fwd_partial — smla_fwd that writes the normalised output in fp32 and
+ * its LSE, for a later LSE-weighted merge of partial results over disjoint
+ * key sets (the DCP path of the vLLM API docs' flashmla_sparse page: each
+ * rank attends to its shard of the top-k set, rows with no key give
+ * (O = 0, LSE = -inf), and the shards are merged by LSE weights; merge them
+ * with smla_combine).  Entries < 0 may sit anywhere in a row (no compaction
+ * needed), exactly as for smla_fwd.
+ *  out_f32  device fp32 [T, h, d_v], 16-byte aligned, written in full.
+ *  lse      device fp32 [T, h], required.
+ * Every other argument is that of smla_fwd.  One top-k range per token, so
+ * no workspace and no allocation; SMLA_ERR_UNSUPPORTED when topk is longer
+ * than one range of the tensor-core kernel the shape uses (2048 positions
+ * for h <= 16, 3072 otherwise).  SMLA_ERR_INVALID_ARG when out_f32 or lse
+ * is NULL or misaligned (T > 0).
+ */
+SMLA_API smla_status smla_fwd_partial(const void* q, const void* kv_cache, int kv_dtype,
+                             const float* k_scale, const int32_t* indices,
+                             const int32_t* valid_len, int T, int h, int d_qk,
+                             int d_v, int topk, int64_t num_slots, float sm_scale,
+                             float* out_f32, float* lse, cudaStream_t stream);
+
+/*
  * smla_fwd_paged — smla_fwd for request-local top-k indices, translated to
  * cache slots inside the kernels' index loads (the fused form of the index
  * conversion the serving backends run as a separate kernel before the

@@ -58,6 +58,8 @@ def load():
         lib.smla_fwd.restype = I
         lib.smla_fwd_ws.argtypes = fwd_args + [P, SZ, P]
         lib.smla_fwd_ws.restype = I
+        lib.smla_fwd_partial.argtypes = fwd_args + [P]
+        lib.smla_fwd_partial.restype = I
         lib.smla_fwd_paged.argtypes = [P, P, I, P, P, P, P, I, I, I, I, P, I, I, I,
                                        I, I, I64, F, P, P, P, SZ, P]
         lib.smla_fwd_paged.restype = I
@@ -92,6 +94,29 @@ def _stream(stream):
 def _check(code, what):
     if code != SMLA_OK:
         raise SmlaError(code, what)
+
+
+def _in_args(q, kv_cache, kv_dtype, k_scale, indices, valid_len, sm_scale,
+             num_slots):
+    """The input arguments of the forward entry points, checked."""
+    import torch
+    assert q.is_cuda and q.dtype == torch.bfloat16 and q.is_contiguous()
+    T, h, d_qk = q.shape
+    assert kv_cache.is_cuda and kv_cache.is_contiguous()
+    if kv_dtype == SMLA_KV_BF16:
+        assert kv_cache.dtype == torch.bfloat16
+    else:
+        assert kv_cache.dtype == torch.uint8
+        assert k_scale is not None and k_scale.dtype == torch.float32
+        assert k_scale.is_cuda and k_scale.is_contiguous()
+    S = kv_cache.numel() // d_qk if num_slots is None else int(num_slots)
+    assert indices.is_cuda and indices.dtype == torch.int32
+    assert indices.is_contiguous() and indices.shape[0] == T
+    if valid_len is not None:
+        assert valid_len.is_cuda and valid_len.dtype == torch.int32
+        assert valid_len.is_contiguous() and valid_len.shape == (T,)
+    return [_p(q), _p(kv_cache), int(kv_dtype), _p(k_scale), _p(indices),
+            _p(valid_len), T, h, d_qk, 512, indices.shape[1], S, float(sm_scale)]
 
 
 def _fwd_args(q, kv_cache, kv_dtype, k_scale, indices, valid_len, sm_scale,
@@ -141,6 +166,25 @@ def smla_fwd(q, kv_cache, kv_dtype, k_scale, indices, valid_len, sm_scale,
     args, out, lse = _fwd_args(q, kv_cache, kv_dtype, k_scale, indices,
                                valid_len, sm_scale, out, lse, num_slots)
     _check(lib.smla_fwd(*args, _stream(stream)), "smla_fwd")
+    return out, lse
+
+
+def smla_fwd_partial(q, kv_cache, kv_dtype, k_scale, indices, valid_len,
+                     sm_scale, out=None, lse=None, num_slots=None, stream=None):
+    """``smla_fwd_partial``: normalised fp32 O [T,h,512] and LSE [T,h] for an
+    LSE-weighted merge (smla_combine).  Returns (out, lse)."""
+    import torch
+    lib = load()
+    T, h, _ = q.shape
+    if out is None:
+        out = torch.empty((T, h, 512), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((T, h), dtype=torch.float32, device=q.device)
+    assert out.dtype == torch.float32 and out.is_contiguous() and out.shape == (T, h, 512)
+    assert lse.dtype == torch.float32 and lse.is_contiguous() and lse.shape == (T, h)
+    args = _in_args(q, kv_cache, kv_dtype, k_scale, indices, valid_len,
+                    sm_scale, num_slots) + [_p(out), _p(lse)]
+    _check(lib.smla_fwd_partial(*args, _stream(stream)), "smla_fwd_partial")
     return out, lse
 
 

@@ -89,7 +89,8 @@ smla_status run_fwd(const void* q, const void* kv, int kv_dtype,
                     const int32_t* valid_len, int T, int h, int d_qk, int d_v,
                     int topk, int64_t num_slots, float sm_scale, void* out,
                     float* lse, void* ws, size_t ws_bytes, bool own_ws,
-                    cudaStream_t stream, const Paged& pg = Paged()) {
+                    cudaStream_t stream, const Paged& pg = Paged(),
+                    float* out_f32 = nullptr) {
   smla_status st = check_args(q, kv, kv_dtype, k_scale, indices, T, h, d_qk,
                               d_v, topk, num_slots, out);
   if (st != SMLA_OK || T == 0) return st;
@@ -106,8 +107,20 @@ smla_status run_fwd(const void* q, const void* kv, int kv_dtype,
     std::lock_guard<std::mutex> lk(g_mutex);
     if ((st = device_info(&dev)) != SMLA_OK) return st;
   }
-  const smla::Plan plan =
+  smla::Plan plan =
       smla::make_plan(T, h, d_qk, d_v, topk, kv_dtype, dev->num_sms);
+  if (out_f32) {
+    // Partial-output mode: one range per token, written straight to the
+    // caller's fp32 buffers (no workspace, no combine).  A top-k longer than
+    // one range of the chosen kernel would need a split: not served.
+    if (plan.kind != smla::kKernelSimt && topk > (plan.kind == smla::kKernelTcKeys
+                                                      ? smla::tc_keys_max_range()
+                                                      : smla::tc_max_range()))
+      return SMLA_ERR_UNSUPPORTED;
+    plan.splits = 1;
+    plan.split_len = topk;
+    plan.workspace_bytes = 0;
+  }
   if (plan.workspace_bytes > 0) {
     if (own_ws) {
       std::lock_guard<std::mutex> lk(g_mutex);
@@ -144,13 +157,17 @@ smla_status run_fwd(const void* q, const void* kv, int kv_dtype,
   p.splits = plan.splits;
   p.split_len = plan.split_len;
   p.sm_scale = sm_scale;
+  p.fp32_out = plan.splits > 1 || out_f32 ? 1 : 0;
   p.req_id = pg.req_id;
   p.block_table = pg.table;
   p.num_reqs = pg.num_reqs;
   p.bt_stride = pg.bt_stride;
   p.block_size = pg.block_size;
   p.block_stride_rows = pg.stride_rows;
-  if (plan.splits > 1) {
+  if (out_f32) {
+    p.o_part = out_f32;
+    p.lse_part = lse;
+  } else if (plan.splits > 1) {
     p.o_part = static_cast<float*>(ws);
     p.lse_part = p.o_part + (size_t)plan.splits * T * h * d_v;
   }
@@ -245,6 +262,19 @@ smla_status smla_fwd_ws(const void* q, const void* kv_cache, int kv_dtype,
   return run_fwd(q, kv_cache, kv_dtype, k_scale, indices, valid_len, T, h,
                  d_qk, d_v, topk, num_slots, sm_scale, out, lse, workspace,
                  workspace_bytes, false, stream);
+}
+
+smla_status smla_fwd_partial(const void* q, const void* kv_cache, int kv_dtype,
+                             const float* k_scale, const int32_t* indices,
+                             const int32_t* valid_len, int T, int h, int d_qk,
+                             int d_v, int topk, int64_t num_slots, float sm_scale,
+                             float* out_f32, float* lse, cudaStream_t stream) {
+  if (T > 0 && (!out_f32 || !lse || !aligned(out_f32, 16) || !aligned(lse, 4)))
+    return SMLA_ERR_INVALID_ARG;
+  // check_args wants a non-NULL bf16 `out`; the fp32 buffer stands in.
+  return run_fwd(q, kv_cache, kv_dtype, k_scale, indices, valid_len, T, h, d_qk,
+                 d_v, topk, num_slots, sm_scale, out_f32, lse, nullptr, 0, false,
+                 stream, Paged(), out_f32);
 }
 
 smla_status smla_fwd_paged(const void* q, const void* kv_cache, int kv_dtype,

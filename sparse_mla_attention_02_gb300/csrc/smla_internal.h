@@ -31,6 +31,9 @@ struct FwdParams {
   int T, h, d_qk, d_v, topk;
   int splits;             // top-k position ranges per (token, head group)
   int split_len;          // positions per range
+  int fp32_out;           // write normalised fp32 O and LSE to o_part / lse_part
+                          // (split s at s * T * h rows): splits > 1, or
+                          // smla_fwd_partial (splits == 1, caller's buffers)
   float sm_scale;
   // Request-local indices (block_table != nullptr): indices hold positions
   // in the token's request; slot = block_table[req, pos / block_size] *

@@ -213,7 +213,7 @@ smla_simt_kernel(FwdParams p, int n_groups) {
     const float inv = empty ? 0.f : 1.f / l;
     const float lse_v = empty ? -INFINITY : m + logf(l);
     const int64_t row = (int64_t)t * p.h + h0 + hh;
-    if (p.splits > 1) {
+    if (p.fp32_out) {
       const int64_t prow = (int64_t)split * p.T * p.h + row;
       float2 o = make_float2(acc[hh][0] * inv, acc[hh][1] * inv);
       *reinterpret_cast<float2*>(p.o_part + prow * p.d_v + c0) = o;

@@ -563,7 +563,7 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
         tmem_wait_ld();
       }
       if (!live) {
-      } else if (p.splits > 1) {
+      } else if (p.fp32_out) {
         float* dst = p.o_part + ((int64_t)split * p.T * p.h + orow) * p.d_v + 256 * r + c;
 #pragma unroll
         for (int k = 0; k < 16; k += 4)
@@ -590,7 +590,7 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
     if (wg == 0 && live && (uint32_t)(i >> 6) == r) {
       const float lse_v =
           empty ? -INFINITY : (m_run + log2f(l_tot)) * 0.69314718055994530942f;
-      if (p.splits > 1)
+      if (p.fp32_out)
         p.lse_part[(int64_t)split * p.T * p.h + orow] = lse_v;
       else if (p.lse)
         p.lse[orow] = lse_v;

@@ -680,7 +680,7 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
         if (hd < p.h) {
           const float o = inv[hd] == 0.f ? 0.f : __uint_as_float(w[hd]) * inv[hd];
           const int64_t orow = (int64_t)t * p.h + hd;
-          if (p.splits > 1)
+          if (p.fp32_out)
             p.o_part[((int64_t)split * p.T * p.h + orow) * p.d_v + ch] = o;
           else
             reinterpret_cast<__nv_bfloat16*>(p.out)[orow * p.d_v + ch] = __float2bfloat16_rn(o);
@@ -696,7 +696,7 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
       const bool empty = !(li > 0.f) || nb == 0;
       const float lse_v = empty ? -INFINITY : (mi + log2f(li)) * 0.69314718055994530942f;
       const int64_t orow = (int64_t)t * p.h + i;
-      if (p.splits > 1)
+      if (p.fp32_out)
         p.lse_part[(int64_t)split * p.T * p.h + orow] = lse_v;
       else if (p.lse)
         p.lse[orow] = lse_v;

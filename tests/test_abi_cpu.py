@@ -132,3 +132,16 @@ def test_paged_bad_arguments_are_rejected_on_the_host(lib, kw, code):
 
 def test_paged_zero_tokens_is_ok(lib):
     assert _fwd_paged(lib, T=0, q=None, kv=None, idx=None, out=None) == 0
+
+
+def test_partial_argument_checks(lib):
+    P = ctypes.c_void_p
+    f = lambda out, lse, T=4, h=16: lib.smla_fwd_partial(
+        P(4096), P(4096), 0, None, P(4096), None, T, h, 576, 512, 64, 256, 0.04,
+        None if out is None else P(out), None if lse is None else P(lse), None)
+    assert f(None, 4096) == 1
+    assert f(4096, None) == 1
+    assert f(4104, 4096) == 1            # fp32 output not 16-byte aligned
+    assert f(4096, 4098) == 1
+    assert f(4096, 4096, h=0) == 1
+    assert f(None, None, T=0) == 0

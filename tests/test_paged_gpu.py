@@ -38,6 +38,7 @@ def paged_view(w, rng, bs, R):
 
 
 def run_both(smla, w, local, req, table, bs, stride_rows=0):
+    smla.smla_get_device_status(clear=True)      # earlier tests may have set it
     wd = w.to("cuda")
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to("cuda")
     O_p, L_p = smla.smla_fwd_paged(wd.q, wd.kv, wd.kv_dtype, wd.k_scale, dev(local),
