@@ -388,6 +388,39 @@ def run_ours(args, rank, world, local_rank):
             del w2, ws2, out2, lse2
             torch.cuda.empty_cache()
 
+        # ---- secondary: group-quantizing E4M3 cache write --------------------
+        # 131072 token rows [kv_c | k_pe] (bf16, 151 MB) written to random
+        # slots of a 262144-slot cache; per row 1152 B read + 576 B codes +
+        # 20 B scales written + 4 B slot id (1752 B), more than L2 per launch.
+        Ncw, Scw = 131072, 262144
+        gcw = torch.Generator(device=dev).manual_seed(4242 + 7919 * rank)
+        kv_c = torch.randn((Ncw, 512), generator=gcw, device=dev).to(torch.bfloat16)
+        k_pe = torch.randn((Ncw, 64), generator=gcw, device=dev).to(torch.bfloat16)
+        slots = torch.randperm(Scw, generator=gcw, device=dev)[:Ncw].int().contiguous()
+        cache = torch.empty((Scw, 576), dtype=torch.uint8, device=dev)
+        scales = torch.empty((Scw, 5), dtype=torch.float32, device=dev)
+
+        def f4():
+            smla.smla_cache_write_e4m3_group(kv_c, k_pe, slots, cache, scales, stream=stream)
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                f4()
+        stream.synchronize()
+        barrier()
+        k4 = max(args.steps, 20)
+        t4 = ranks_max(time_steps(f4, k4, stream)) / k4
+        b4 = Ncw * (2 * 576 + 576 + 4 * 5 + 4)
+        secondary["fp8_group_cache_write"] = {
+            "rows_per_s": round(world * Ncw / t4, 1),
+            "ms_per_step": round(1e3 * t4, 4),
+            "hbm_gbs": round(b4 / t4 / 1e9, 1),
+            "frac_hbm": round(b4 / t4 / 1e9 / pk["hbm_gbs"], 4),
+            "bytes_per_row": 1752,
+            "kernel": "smla_cache_write_kernel",
+        }
+        del kv_c, k_pe, slots, cache, scales
+        torch.cuda.empty_cache()
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s",

@@ -151,6 +151,34 @@ SMLA_API smla_status smla_fwd_ws(const void* q, const void* kv_cache, int kv_dty
                         size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * smla_cache_write_e4m3_group — write token rows into an E4M3 cache with one
+ * fp32 scale per (slot, 128-channel group), the layout smla_fwd reads for
+ * SMLA_KV_FP8_E4M3_GROUP128.  The flashinfer_mla_sparse_sm90.py page reads
+ * that layout (ckv_scale_arr) but notes the cache-write op producing it is
+ * missing; vLLM's concat_and_cache_mla (same pages) is the write for the
+ * other formats: row [kv_c | k_pe] at the token's slot.  For each written
+ * row and group g (channels [128 g, 128 g + 128)):
+ *   scale = amax|x| / 448 in fp32 (1 for an all-zero group)
+ *   code  = e4m3(x / scale), fp32 division, round to nearest even,
+ *           saturating at +-448
+ *  kv_c          device bf16 [N, 512], 16-byte aligned
+ *  k_pe          device bf16 [N, 64] for d_qk = 576, NULL for d_qk = 512
+ *  slot_mapping  device int32 [N]: the cache row of each token; < 0 = skip;
+ *                >= num_slots = skip and set SMLA_ERR_BAD_INDEX (device status)
+ *  kv_cache      device uint8 [num_slots, d_qk], 16-byte aligned
+ *  scales        device fp32 [num_slots, ceil(d_qk / 128)]
+ * Rows not written keep their bytes and scales.  Asynchronous on `stream`,
+ * no allocation.  Errors: SMLA_ERR_INVALID_ARG (N < 0, num_slots < 1, NULL
+ * or misaligned pointers, k_pe given for d_qk = 512 or missing for 576),
+ * SMLA_ERR_UNSUPPORTED (d_qk not 512 or 576), SMLA_ERR_CUDA.  N = 0 is OK.
+ */
+SMLA_API smla_status smla_cache_write_e4m3_group(const void* kv_c, const void* k_pe,
+                                                 const int32_t* slot_mapping, int N,
+                                                 int d_qk, int64_t num_slots,
+                                                 void* kv_cache, float* scales,
+                                                 cudaStream_t stream);
+
+/*
  * smla_fwd_partial — smla_fwd that writes the normalised output in fp32 and
  * its LSE, for a later LSE-weighted merge of partial results over disjoint
  * key sets (the DCP path of the vLLM API docs' flashmla_sparse page: each

@@ -182,3 +182,59 @@ def paged_to_global(token_indices, req_id, block_table, block_size,
                 continue
             out[t, j] = blk * stride + e % block_size
     return out
+
+
+def _e4m3_positive_values():
+    """Values of the codes 0x00..0x7E (0x7F is NaN), ascending."""
+    return np.array([e4m3_to_f64(c) for c in range(0x7F)], dtype=np.float64)
+
+
+def e4m3_encode(v):
+    """float32 values -> E4M3 ("fn") codes, round to nearest with ties to the
+    even code, saturating at +-448 (the satfinite conversion); the sign is
+    kept for values that round to zero.  Written from the format's value
+    list, not from a conversion routine."""
+    vals = _e4m3_positive_values()
+    v = np.asarray(v, dtype=np.float32).astype(np.float64)
+    a = np.abs(v)
+    i = np.clip(np.searchsorted(vals, a, side="right") - 1, 0, len(vals) - 1)
+    j = np.minimum(i + 1, len(vals) - 1)
+    lo, hi = vals[i], vals[j]
+    d_lo, d_hi = a - lo, hi - a
+    code = np.where(d_lo < d_hi, i, j)
+    tie = d_lo == d_hi
+    code = np.where(tie, np.where(i % 2 == 0, i, j), code)
+    code = np.where(a >= vals[-1], len(vals) - 1, code).astype(np.uint8)
+    return np.where(np.signbit(v), code | 0x80, code).astype(np.uint8)
+
+
+def cache_write_e4m3_group(kv_c_bits, k_pe_bits, slot_mapping, cache, scales):
+    """The group-quantizing E4M3 cache write (test infrastructure).
+
+    The flashinfer_mla_sparse_sm90.py page reads the per-token x
+    128-channel-group scale layout (``ckv_scale_arr``) but notes that the
+    cache-write op producing it is missing; vLLM's concat_and_cache_mla
+    (same pages) writes a token's [kv_c | k_pe] row at its slot.  Reading:
+    for each written row and group g (channels [128 g, 128 g + 128)),
+    scale = amax|x| / 448 in fp32 (1 for an all-zero group) and
+    code = e4m3(x / scale) (fp32 division, round to nearest even,
+    saturating).  Rows with slot < 0 or >= num_slots are not written.
+    kv_c_bits: uint16 bf16 bits [N, 512]; k_pe_bits: [N, d_qk - 512] or
+    None; cache: uint8 [S, d_qk] (updated in place); scales: fp32 [S, G].
+    """
+    kv = np.asarray(kv_c_bits, dtype=np.uint16)
+    rows = kv if k_pe_bits is None else np.concatenate(
+        [kv, np.asarray(k_pe_bits, dtype=np.uint16)], axis=1)
+    x_all = (rows.astype(np.uint32) << 16).view(np.float32)
+    S, d_qk = cache.shape
+    G = (d_qk + 127) // 128
+    for n, s in enumerate(np.asarray(slot_mapping, dtype=np.int64)):
+        if s < 0 or s >= S:
+            continue
+        for g in range(G):
+            x = x_all[n, 128 * g: min(128 * g + 128, d_qk)]
+            amax = np.float32(np.max(np.abs(x)))
+            scale = np.float32(amax) / np.float32(448.0) if amax > 0 else np.float32(1.0)
+            cache[s, 128 * g: 128 * g + x.size] = e4m3_encode(x / scale)
+            scales[s, g] = scale
+    return cache, scales

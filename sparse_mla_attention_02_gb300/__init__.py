@@ -58,6 +58,8 @@ def load():
         lib.smla_fwd.restype = I
         lib.smla_fwd_ws.argtypes = fwd_args + [P, SZ, P]
         lib.smla_fwd_ws.restype = I
+        lib.smla_cache_write_e4m3_group.argtypes = [P, P, P, I, I, I64, P, P, P]
+        lib.smla_cache_write_e4m3_group.restype = I
         lib.smla_fwd_partial.argtypes = fwd_args + [P]
         lib.smla_fwd_partial.restype = I
         lib.smla_fwd_paged.argtypes = [P, P, I, P, P, P, P, I, I, I, I, P, I, I, I,
@@ -167,6 +169,30 @@ def smla_fwd(q, kv_cache, kv_dtype, k_scale, indices, valid_len, sm_scale,
                                valid_len, sm_scale, out, lse, num_slots)
     _check(lib.smla_fwd(*args, _stream(stream)), "smla_fwd")
     return out, lse
+
+
+def smla_cache_write_e4m3_group(kv_c, k_pe, slot_mapping, kv_cache, scales,
+                                stream=None):
+    """``smla_cache_write_e4m3_group``: quantize token rows [kv_c | k_pe]
+    (bf16 [N,512] and [N,64], or k_pe None for 512-channel rows) into the
+    E4M3 cache (uint8 [S, d_qk]) with one fp32 scale per (slot, 128-channel
+    group) (scales [S, ceil(d_qk/128)]) at rows slot_mapping (int32 [N];
+    negative = skip)."""
+    import torch
+    lib = load()
+    N = kv_c.shape[0]
+    for x in (kv_c, k_pe):
+        if x is not None:
+            assert x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous()
+    assert kv_c.shape == (N, 512)
+    d_qk = 512 if k_pe is None else 512 + k_pe.shape[1]
+    assert slot_mapping.dtype == torch.int32 and slot_mapping.shape == (N,)
+    assert kv_cache.dtype == torch.uint8 and kv_cache.shape[1] == d_qk
+    assert scales.dtype == torch.float32 and scales.shape == (kv_cache.shape[0], (d_qk + 127) // 128)
+    _check(lib.smla_cache_write_e4m3_group(_p(kv_c), _p(k_pe), _p(slot_mapping), N, d_qk,
+                                           kv_cache.shape[0], _p(kv_cache), _p(scales),
+                                           _stream(stream)), "smla_cache_write_e4m3_group")
+    return kv_cache, scales
 
 
 def smla_fwd_partial(q, kv_cache, kv_dtype, k_scale, indices, valid_len,

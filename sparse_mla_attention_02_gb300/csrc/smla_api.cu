@@ -264,6 +264,30 @@ smla_status smla_fwd_ws(const void* q, const void* kv_cache, int kv_dtype,
                  workspace_bytes, false, stream);
 }
 
+smla_status smla_cache_write_e4m3_group(const void* kv_c, const void* k_pe,
+                                       const int32_t* slot_mapping, int N, int d_qk,
+                                       int64_t num_slots, void* kv_cache, float* scales,
+                                       cudaStream_t stream) {
+  if (N < 0 || num_slots < 1) return SMLA_ERR_INVALID_ARG;
+  if (d_qk != 512 && d_qk != 576) return SMLA_ERR_UNSUPPORTED;
+  if (N == 0) return SMLA_OK;
+  if (!kv_c || !slot_mapping || !kv_cache || !scales || (d_qk == 576) != (k_pe != nullptr))
+    return SMLA_ERR_INVALID_ARG;
+  if (!aligned(kv_c, 16) || (k_pe && !aligned(k_pe, 16)) || !aligned(kv_cache, 16) ||
+      !aligned(scales, 4) || !aligned(slot_mapping, 4))
+    return SMLA_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    const smla_status st = device_info(&dev);
+    if (st != SMLA_OK) return st;
+  }
+  return smla::launch_cache_write(kv_c, k_pe, slot_mapping, N, d_qk, num_slots, kv_cache,
+                                  scales, dev->status, stream) == cudaSuccess
+             ? SMLA_OK
+             : SMLA_ERR_CUDA;
+}
+
 smla_status smla_fwd_partial(const void* q, const void* kv_cache, int kv_dtype,
                              const float* k_scale, const int32_t* indices,
                              const int32_t* valid_len, int T, int h, int d_qk,

@@ -102,6 +102,9 @@ cudaError_t launch_tc(const FwdParams& p, cudaStream_t stream);
 bool tc_keys_supported(int h, int d_qk, int kv_format);
 int tc_keys_max_range();
 cudaError_t launch_tc_keys(const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_cache_write(const void* kv_c, const void* k_pe, const int32_t* slot,
+                               int N, int d_qk, int64_t num_slots, void* cache,
+                               float* scales, int* status, cudaStream_t stream);
 cudaError_t launch_combine(const float* o_parts, const float* lse_parts,
                            int n_parts, int64_t rows, int d_v, void* out,
                            float* lse, cudaStream_t stream);

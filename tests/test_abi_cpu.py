@@ -145,3 +145,24 @@ def test_partial_argument_checks(lib):
     assert f(4096, 4098) == 1
     assert f(4096, 4096, h=0) == 1
     assert f(None, None, T=0) == 0
+
+
+def test_cache_write_argument_checks(lib):
+    P = ctypes.c_void_p
+    f = lambda kv=4096, pe=4096, sl=4096, N=4, d=576, S=64, c=4096, sc=4096: \
+        lib.smla_cache_write_e4m3_group(
+            None if kv is None else P(kv), None if pe is None else P(pe),
+            None if sl is None else P(sl), N, d, S, None if c is None else P(c),
+            None if sc is None else P(sc), None)
+    assert f(N=-1) == 1
+    assert f(S=0) == 1
+    assert f(d=640) == 2
+    assert f(N=0, kv=None, pe=None, sl=None, c=None, sc=None) == 0
+    assert f(kv=None) == 1
+    assert f(sl=None) == 1
+    assert f(c=None) == 1
+    assert f(sc=None) == 1
+    assert f(pe=None) == 1               # 576-channel rows need k_pe
+    assert f(d=512) == 1                 # 512-channel rows take no k_pe
+    assert f(kv=4104) == 1               # misaligned
+    assert f(c=4104) == 1

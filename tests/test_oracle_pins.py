@@ -378,3 +378,69 @@ def test_paged_masks_what_cannot_be_translated():
     assert out.tolist() == [[64, 69, 79, -1, 120, 127, -1, -1]]
     assert oracle.paged_to_global(idx, [1], table, 16).tolist() == [[-1] * 8]
     assert oracle.paged_to_global(idx, [-1], table, 16).tolist() == [[-1] * 8]
+
+
+# ---- E4M3 encoding and the group-quantizing cache write ---------------------
+
+
+def test_e4m3_encode_round_trips_every_code():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    vals = np.array([oracle.e4m3_to_f64(int(c)) for c in codes])
+    assert np.array_equal(oracle.e4m3_encode(vals.astype(np.float32)), codes)
+
+
+def test_e4m3_encode_midpoints_go_to_the_even_code():
+    vals = np.array([oracle.e4m3_to_f64(c) for c in range(0x7F)])
+    mid = ((vals[:-1] + vals[1:]) / 2).astype(np.float32)
+    assert np.array_equal(mid.astype(np.float64), (vals[:-1] + vals[1:]) / 2)  # exact in fp32
+    got = oracle.e4m3_encode(mid)
+    want = np.where(np.arange(126) % 2 == 0, np.arange(126), np.arange(1, 127))
+    assert np.array_equal(got, want.astype(np.uint8))
+
+
+def test_e4m3_encode_agrees_with_torch_and_saturates():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(0)
+    x = np.concatenate([rng.uniform(-460, 460, 20000), rng.normal(0, 1, 20000),
+                        rng.normal(0, 0.01, 5000)]).astype(np.float32)
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_encode(x), want)
+    big = np.array([448.0, 470.0, 1e6, -1e30, np.inf], dtype=np.float32)
+    assert oracle.e4m3_encode(big).tolist() == [0x7E, 0x7E, 0x7E, 0xFE, 0x7E]
+
+
+def test_cache_write_quantizes_within_the_format_bound():
+    rng = np.random.default_rng(1)
+    N, S = 40, 64
+    kv = rng.normal(0, 1, (N, 512)).astype(np.float32)
+    pe = rng.normal(0, 3, (N, 64)).astype(np.float32)
+    kv[3, 128:256] = 0.0                                      # an all-zero group
+    bits = lambda a: (a.view(np.uint32) >> 16).astype(np.uint16)   # exact: truncate to bf16 below
+    kv = (bits(kv).astype(np.uint32) << 16).view(np.float32)
+    pe = (bits(pe).astype(np.uint32) << 16).view(np.float32)
+    slots = rng.permutation(S)[:N].astype(np.int64)
+    slots[5] = -1
+    cache = np.full((S, 576), 0xAA, dtype=np.uint8)
+    scales = np.full((S, 5), -1.0, dtype=np.float32)
+    oracle.cache_write_e4m3_group(bits(kv), bits(pe), slots, cache, scales)
+    rows = np.concatenate([kv, pe], axis=1).astype(np.float64)
+    for n, s in enumerate(slots):
+        if s < 0:
+            continue
+        for g in range(5):
+            sl = slice(128 * g, min(128 * g + 128, 576))
+            x = rows[n, sl]
+            sc = float(scales[s, g])
+            dq = np.array([oracle.e4m3_to_f64(int(b)) for b in cache[s, sl]]) * sc
+            amax = np.abs(x).max()
+            if amax == 0:
+                assert sc == 1.0 and np.all(cache[s, sl] == 0)
+                continue
+            assert sc == np.float32(amax) / np.float32(448)
+            # relative E4M3 spacing is at most 2^-3: error <= half of it at |x|,
+            # or half the subnormal step 2^-9 * scale
+            bound = np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -10 * sc) * (1 + 1e-6)
+            assert np.all(np.abs(dq - x) <= bound)
+            assert np.max(np.abs(dq)) == pytest.approx(448 * sc, rel=1e-6)
+    untouched = np.setdiff1d(np.arange(S), slots[slots >= 0])
+    assert np.all(cache[untouched] == 0xAA) and np.all(scales[untouched] == -1.0)
