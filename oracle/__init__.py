@@ -27,6 +27,9 @@ _lock = threading.Lock()
 KV_BF16 = 0
 KV_E4M3 = 1
 KV_E4M3_GROUP128 = 2
+KV_FP8_DS_MLA = 3          # 656-byte rows: 512 E4M3 | 4 fp32 scales | 64 bf16
+KV_E4M3_GROUP4_KPE = 4     # E4M3 [S, 576], scales [S, 4] (ckv), one kpe scale
+DS_MLA_ROW_BYTES = 656
 
 
 def build(force: bool = False) -> str:
@@ -53,7 +56,7 @@ def _load():
         P = ctypes.c_void_p
         lib.smla_oracle_fwd.restype = ctypes.c_int
         lib.smla_oracle_fwd.argtypes = [
-            P, P, ctypes.c_int, P, P, P, ctypes.c_int64, ctypes.c_int,
+            P, P, ctypes.c_int, P, ctypes.c_float, P, P, ctypes.c_int64, ctypes.c_int,
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
             ctypes.c_double, P, ctypes.c_int64, P, P, ctypes.c_int]
         lib.smla_oracle_merge.restype = None
@@ -85,13 +88,16 @@ def default_threads() -> int:
 
 def sparse_mla_fwd(q_bits, kv, kv_dtype, k_scale, indices, valid_len,
                    sm_scale, d_v=512, num_slots=None, tokens=None,
-                   n_threads=None):
+                   n_threads=None, kpe_scale=1.0):
     """Oracle forward.
 
     q_bits    uint16 [T, h, d_qk]  (bf16 bit patterns)
-    kv        uint16 [S, d_qk] (bf16 bits) or uint8 [S, d_qk] (E4M3 bytes)
-    kv_dtype  KV_BF16 / KV_E4M3 / KV_E4M3_GROUP128
-    k_scale   float32 [1] or [S, ceil(d_qk/128)] or None
+    kv        uint16 [S, d_qk] (bf16 bits), uint8 [S, d_qk] (E4M3 bytes) or
+              uint8 [S, 656] (KV_FP8_DS_MLA rows)
+    kv_dtype  KV_BF16 / KV_E4M3 / KV_E4M3_GROUP128 / KV_FP8_DS_MLA /
+              KV_E4M3_GROUP4_KPE
+    k_scale   float32 [1], [S, ceil(d_qk/128)], [S, 4] (KV_E4M3_GROUP4_KPE) or None
+    kpe_scale the rope channels' scale (KV_E4M3_GROUP4_KPE only)
     indices   int32 [T, topk];  valid_len int32 [T] or None
     tokens    optional int64 list of token ids (rows of the result follow it)
     Returns (O float64 [n, h, d_v], LSE float64 [n, h]).
@@ -100,7 +106,8 @@ def sparse_mla_fwd(q_bits, kv, kv_dtype, k_scale, indices, valid_len,
     q_bits = np.ascontiguousarray(q_bits, dtype=np.uint16)
     T, h, d_qk = q_bits.shape
     want = np.uint16 if kv_dtype == KV_BF16 else np.uint8
-    kv = np.ascontiguousarray(kv, dtype=want).reshape(-1, d_qk)
+    row = DS_MLA_ROW_BYTES if kv_dtype == KV_FP8_DS_MLA else d_qk
+    kv = np.ascontiguousarray(kv, dtype=want).reshape(-1, row)
     S = kv.shape[0] if num_slots is None else int(num_slots)
     indices = np.ascontiguousarray(indices, dtype=np.int32)
     assert indices.shape[0] == T
@@ -118,7 +125,8 @@ def sparse_mla_fwd(q_bits, kv, kv_dtype, k_scale, indices, valid_len,
     out = np.zeros((n, h, d_v), dtype=np.float64)
     lse = np.zeros((n, h), dtype=np.float64)
     rc = lib.smla_oracle_fwd(
-        _ptr(q_bits), _ptr(kv), int(kv_dtype), _ptr(k_scale), _ptr(indices),
+        _ptr(q_bits), _ptr(kv), int(kv_dtype), _ptr(k_scale), float(kpe_scale),
+        _ptr(indices),
         _ptr(valid_len), T, h, d_qk, int(d_v), topk, S, float(sm_scale),
         _ptr(tokens), n, _ptr(out), _ptr(lse),
         int(n_threads or default_threads()))

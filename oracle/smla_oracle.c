@@ -32,12 +32,21 @@
  *    directly, per-tensor k_scale, per-token x 128-channel-group scales
  *    (ckv_scale_arr); the valid entries form a compacted prefix with -1 past it
  *    (forward_mqa comment on return_valid_counts).
+ *  - same page, forward_mqa: the FP8 cache is handed to the kernel as ckv =
+ *    row[:512] and kpe = row[512:] with ckv_scale = k_scale and a separate
+ *    kpe_scale (format 4 below: four ckv group scales per slot and one
+ *    per-tensor kpe scale).
+ *  - same diff, cutlass_fa3_sparse.py module docstring: the FlashMLA FP8
+ *    cache (fp8_ds_mla) takes 656 bytes per token (format 3 below).
  *
  * Readings where the pages are silent (listed with the others in the design
  * notes): natural-log LSE; a -1 (or out-of-range id) inside the valid prefix is
  * masked; valid_len > topk is clamped; duplicates each count once; E4M3 is the
  * "fn" variant (no Inf, S.1111.111 = NaN), as torch.float8_e4m3fn; the group
- * scale of channel c is k_scale[idx * ceil(d_qk/128) + c/128].
+ * scale of channel c is k_scale[idx * ceil(d_qk/128) + c/128].  The 656-byte
+ * fp8_ds_mla row (its layout is not printed on the pages) is read as
+ * [512 E4M3 bytes | 4 fp32 scales, one per 128-channel group, little-endian |
+ * 64 bf16 rope values, little-endian]: 512 + 16 + 128 = 656.
  *
  * Precision: every input value is exactly representable in fp64, so the only
  * rounding is fp64 arithmetic.  Threads (POSIX) split the token list; each
@@ -50,7 +59,14 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORACLE_KV_BF16 = 0, ORACLE_KV_E4M3 = 1, ORACLE_KV_E4M3_GROUP128 = 2 };
+enum {
+  ORACLE_KV_BF16 = 0,
+  ORACLE_KV_E4M3 = 1,
+  ORACLE_KV_E4M3_GROUP128 = 2,
+  ORACLE_KV_FP8_DS_MLA = 3,      /* 656-byte rows, scales and rope inside the row */
+  ORACLE_KV_E4M3_GROUP4_KPE = 4  /* E4M3 [S, 576]; scales [S, 4] for ckv, one kpe scale */
+};
+enum { ORACLE_DS_MLA_ROW = 656 };
 
 /* bf16 -> fp64: a bf16 value is the upper half of an IEEE binary32. */
 double smla_oracle_bf16_to_f64(uint16_t bits) {
@@ -81,6 +97,7 @@ typedef struct {
   const void* kv;
   int kv_dtype;
   const float* k_scale;
+  double kpe_scale;
   const int32_t* indices;
   const int32_t* valid_len;
   int64_t T;
@@ -101,10 +118,21 @@ static double kv_value(const oracle_job* jb, int64_t slot, int c) {
   if (jb->kv_dtype == ORACLE_KV_BF16) {
     const uint16_t* row = (const uint16_t*)jb->kv + slot * (int64_t)jb->d_qk;
     return smla_oracle_bf16_to_f64(row[c]);
+  } else if (jb->kv_dtype == ORACLE_KV_FP8_DS_MLA) {
+    const uint8_t* row = (const uint8_t*)jb->kv + slot * (int64_t)ORACLE_DS_MLA_ROW;
+    if (c < 512) {
+      float sc;
+      memcpy(&sc, row + 512 + 4 * (c / 128), sizeof sc);
+      return smla_oracle_e4m3_to_f64(row[c]) * (double)sc;
+    }
+    uint16_t b = (uint16_t)(row[528 + 2 * (c - 512)] | (row[529 + 2 * (c - 512)] << 8));
+    return smla_oracle_bf16_to_f64(b);
   } else {
     const uint8_t* row = (const uint8_t*)jb->kv + slot * (int64_t)jb->d_qk;
     double x = smla_oracle_e4m3_to_f64(row[c]);
     if (jb->kv_dtype == ORACLE_KV_E4M3) return x * (double)jb->k_scale[0];
+    if (jb->kv_dtype == ORACLE_KV_E4M3_GROUP4_KPE)
+      return c < 512 ? x * (double)jb->k_scale[slot * 4 + c / 128] : x * jb->kpe_scale;
     int G = (jb->d_qk + 127) / 128;
     return x * (double)jb->k_scale[slot * G + c / 128];
   }
@@ -184,23 +212,30 @@ static void* oracle_worker(void* arg) {
 /*
  * smla_oracle_fwd — the forward for a list of tokens.
  *   q        bf16 bits [T, h, d_qk]
- *   kv       bf16 bits [num_slots, d_qk] (kv_dtype 0) or E4M3 bytes (1, 2)
- *   k_scale  kv_dtype 1: [1]; kv_dtype 2: [num_slots, ceil(d_qk/128)]; else unused
+ *   kv       bf16 bits [num_slots, d_qk] (kv_dtype 0), E4M3 bytes
+ *            [num_slots, d_qk] (1, 2, 4) or 656-byte rows [num_slots, 656] (3)
+ *   k_scale  kv_dtype 1: [1]; 2: [num_slots, ceil(d_qk/128)]; 4: [num_slots, 4];
+ *            else unused
+ *   kpe_scale  kv_dtype 4: the scale of the 64 rope channels (fp32, like every
+ *            other scale); else unused
  *   indices  int32 [T, topk];  valid_len int32 [T] or NULL
  *   tokens   token ids to evaluate (NULL: 0..T-1, then n_tokens must be T)
  *   out      fp64 [n_tokens, h, d_v];  lse fp64 [n_tokens, h]
  * Returns 0 on success, 1 on a bad argument, 3 if a thread could not allocate.
  */
 int smla_oracle_fwd(const uint16_t* q, const void* kv, int kv_dtype,
-                    const float* k_scale, const int32_t* indices,
+                    const float* k_scale, float kpe_scale, const int32_t* indices,
                     const int32_t* valid_len, int64_t T, int h, int d_qk,
                     int d_v, int topk, int64_t num_slots, double sm_scale,
                     const int64_t* tokens, int64_t n_tokens, double* out,
                     double* lse, int n_threads) {
   if (!q || !kv || !indices || !out || !lse) return 1;
   if (T < 0 || h < 1 || d_qk < 1 || d_v < 1 || d_v > d_qk || topk < 1) return 1;
-  if (kv_dtype < 0 || kv_dtype > 2) return 1;
-  if (kv_dtype != ORACLE_KV_BF16 && !k_scale) return 1;
+  if (kv_dtype < 0 || kv_dtype > 4) return 1;
+  if ((kv_dtype == ORACLE_KV_E4M3 || kv_dtype == ORACLE_KV_E4M3_GROUP128 ||
+       kv_dtype == ORACLE_KV_E4M3_GROUP4_KPE) && !k_scale) return 1;
+  if ((kv_dtype == ORACLE_KV_FP8_DS_MLA || kv_dtype == ORACLE_KV_E4M3_GROUP4_KPE) &&
+      d_qk != 576) return 1;
   if (!tokens && n_tokens != T) return 1;
   if (tokens)
     for (int64_t i = 0; i < n_tokens; ++i)
@@ -209,6 +244,7 @@ int smla_oracle_fwd(const uint16_t* q, const void* kv, int kv_dtype,
   oracle_job jb;
   memset(&jb, 0, sizeof jb);
   jb.q = q; jb.kv = kv; jb.kv_dtype = kv_dtype; jb.k_scale = k_scale;
+  jb.kpe_scale = (double)kpe_scale;
   jb.indices = indices; jb.valid_len = valid_len; jb.T = T; jb.h = h;
   jb.d_qk = d_qk; jb.d_v = d_v; jb.topk = topk; jb.num_slots = num_slots;
   jb.sm_scale = sm_scale; jb.tokens = tokens; jb.n_tokens = n_tokens;

@@ -12,6 +12,12 @@ Recipes (the readings behind them are listed in the design notes):
 * FP8 group cache: scales ~ U[lo, hi] per (slot, 128-channel group); stored
   byte = e4m3(clamp(N(0,1)/scale[slot, c // 128], +-448)).  The E4M3 encoder
   is torch's float -> float8_e4m3fn cast (round to nearest even).
+* fp8_ds_mla 656-byte rows: the 512 ckv channels as in the group cache (four
+  scales per slot), packed as [512 code bytes | 4 fp32 scales | 64 bf16 rope
+  values N(0,1)], little-endian.
+* E4M3 with four ckv group scales and one kpe scale: ckv codes as in the
+  group cache (four scales per slot), rope codes as in the per-tensor cache
+  with kpe_scale.
 * Index rows: distinct slot ids in random order for the valid prefix, -1 past
   it (vLLM "Sparse MLA on Hopper" test file: randperm rows, -1 tails;
   flashinfer_mla_sparse_sm90.py, forward_mqa: compacted prefix, -1 past it).
@@ -30,6 +36,9 @@ import torch
 KV_BF16 = 0
 KV_FP8_E4M3 = 1
 KV_FP8_E4M3_GROUP128 = 2
+KV_FP8_DS_MLA = 3
+KV_FP8_E4M3_GROUP4_KPE = 4
+DS_MLA_ROW_BYTES = 656
 
 E4M3_MAX = 448.0
 
@@ -52,6 +61,7 @@ class Workload:
     valid_len: torch.Tensor    # int32 [T]
     real_heads: int = 0        # heads that carry data (pad heads excluded)
     notes: dict = field(default_factory=dict)
+    kpe_scale: float = 1.0     # rope scale of KV_FP8_E4M3_GROUP4_KPE
 
     def to(self, device) -> "Workload":
         mv = lambda x: None if x is None else x.to(device)
@@ -59,7 +69,8 @@ class Workload:
                         self.topk, self.num_slots, self.kv_dtype,
                         self.sm_scale, mv(self.q), mv(self.kv),
                         mv(self.k_scale), mv(self.indices),
-                        mv(self.valid_len), self.real_heads, dict(self.notes))
+                        mv(self.valid_len), self.real_heads, dict(self.notes),
+                        self.kpe_scale)
 
 
 def _gen(device, seed):
@@ -103,6 +114,14 @@ def fp8_cache_group(S, d, scales, device, gen, chunk_rows=1 << 18):
         x = x / scales[s:e][:, grp]
         out[s:e] = e4m3_bytes(x)
     return out
+
+
+def ds_mla_rows(codes: torch.Tensor, scales: torch.Tensor, rope: torch.Tensor) -> torch.Tensor:
+    """Pack [512 E4M3 bytes | 4 fp32 scales | 64 bf16] into 656-byte rows."""
+    S = codes.shape[0]
+    assert codes.shape == (S, 512) and scales.shape == (S, 4) and rope.shape == (S, 64)
+    return torch.cat([codes, scales.float().contiguous().view(torch.uint8),
+                      rope.to(torch.bfloat16).contiguous().view(torch.uint8)], dim=1).contiguous()
 
 
 def index_rows(rng: np.random.Generator, T, topk, valid, pick):
@@ -254,8 +273,22 @@ def custom(T, h, d_qk=576, d_v=512, topk=64, num_slots=256, kv_dtype=KV_BF16,
     q = bf16_normal((T, h, d_qk), device, g)
     G = (d_qk + 127) // 128
     scales = None
+    kpe_scale = 1.0
     if kv_dtype == KV_BF16:
         kv = bf16_normal((num_slots, d_qk), device, g)
+    elif kv_dtype in (KV_FP8_DS_MLA, KV_FP8_E4M3_GROUP4_KPE):
+        assert d_qk == 576
+        lo, hi = scale_range
+        scales = (torch.rand((num_slots, 4), generator=g, device=device)
+                  * (hi - lo) + lo).float()
+        codes = fp8_cache_group(num_slots, 512, scales, device, g)
+        if kv_dtype == KV_FP8_DS_MLA:
+            kv = ds_mla_rows(codes, scales, bf16_normal((num_slots, 64), device, g))
+            scales = None
+        else:
+            kpe_scale = float(k_scale)
+            kv = torch.cat([codes, fp8_cache_per_tensor(num_slots, 64, kpe_scale, device, g)],
+                           dim=1).contiguous()
     elif kv_dtype == KV_FP8_E4M3:
         kv = fp8_cache_per_tensor(num_slots, d_qk, k_scale, device, g)
         scales = torch.tensor([k_scale], dtype=torch.float32, device=device)
@@ -275,7 +308,7 @@ def custom(T, h, d_qk=576, d_v=512, topk=64, num_slots=256, kv_dtype=KV_BF16,
     return Workload(name, T, h, d_qk, d_v, topk, num_slots, kv_dtype,
                     (1.0 / math.sqrt(d_qk)) if sm_scale is None else sm_scale,
                     q, kv, scales, torch.from_numpy(idx).to(device),
-                    torch.from_numpy(valid).to(device), h)
+                    torch.from_numpy(valid).to(device), h, kpe_scale=kpe_scale)
 
 
 def token_subset(w: Workload, sel, device="cpu") -> Workload:

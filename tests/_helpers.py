@@ -25,7 +25,7 @@ def oracle_fwd(w, tokens=None, valid=True, n_threads=None, indices=None):
     return oracle.sparse_mla_fwd(bits16(w.q), kv_numpy(w), w.kv_dtype, ks, idx,
                                  vl, w.sm_scale, d_v=w.d_v,
                                  num_slots=w.num_slots, tokens=tokens,
-                                 n_threads=n_threads)
+                                 n_threads=n_threads, kpe_scale=w.kpe_scale)
 
 
 def dequant_rows_torch(w) -> torch.Tensor:
@@ -33,7 +33,17 @@ def dequant_rows_torch(w) -> torch.Tensor:
     library route independent of the oracle's decoder)."""
     if w.kv.dtype == torch.bfloat16:
         return w.kv.cpu().to(torch.float64)
+    if w.kv_dtype == 3:                       # 656-byte rows
+        rows = w.kv.cpu()
+        codes = rows[:, :512].contiguous().view(torch.float8_e4m3fn).to(torch.float64)
+        sc = rows[:, 512:528].contiguous().view(torch.float32).to(torch.float64)
+        rope = rows[:, 528:656].contiguous().view(torch.bfloat16).to(torch.float64)
+        return torch.cat([codes * sc[:, torch.arange(512) // 128], rope], dim=1)
     x = w.kv.cpu().view(torch.float8_e4m3fn).to(torch.float64)
+    if w.kv_dtype == 4:                       # 4 ckv group scales + kpe scale
+        sc = w.k_scale.cpu().to(torch.float64)
+        return torch.cat([x[:, :512] * sc[:, torch.arange(512) // 128],
+                          x[:, 512:] * w.kpe_scale], dim=1)
     if w.kv_dtype == 1:
         return x * float(w.k_scale.cpu()[0])
     grp = torch.arange(w.d_qk) // 128

@@ -278,7 +278,8 @@ def _brute(q, K, idx, v, sm_scale, S):
 
 
 @pytest.mark.parametrize("kv_dtype", [W.KV_BF16, W.KV_FP8_E4M3,
-                                      W.KV_FP8_E4M3_GROUP128])
+                                      W.KV_FP8_E4M3_GROUP128, W.KV_FP8_DS_MLA,
+                                      W.KV_FP8_E4M3_GROUP4_KPE])
 def test_brute_force_tiny(kv_dtype):
     w = W.custom(T=2, h=2, topk=8, num_slots=24, kv_dtype=kv_dtype,
                  valid=[8, 3], seed=21, sm_scale=0.02, k_scale=0.5,
@@ -444,3 +445,77 @@ def test_cache_write_quantizes_within_the_format_bound():
             assert np.max(np.abs(dq)) == pytest.approx(448 * sc, rel=1e-6)
     untouched = np.setdiff1d(np.arange(S), slots[slots >= 0])
     assert np.all(cache[untouched] == 0xAA) and np.all(scales[untouched] == -1.0)
+
+
+# ------------------------------------------------------- layout variants --
+
+def _e4m3_torch(b: int) -> float:
+    return float(torch.tensor([b], dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64))
+
+
+@pytest.mark.parametrize("kv_dtype", [W.KV_FP8_DS_MLA, W.KV_FP8_E4M3_GROUP4_KPE])
+def test_layout_variant_channels_read_the_right_bytes(kv_dtype):
+    """One-hot q at channel c, one key: LSE = sm_scale * K[c], K[c] decoded
+    here from the row's own bytes with struct and torch's E4M3 cast.
+    656-byte row: c < 512 -> e4m3(byte c) * fp32 at bytes 512 + 4 (c // 128);
+    c >= 512 -> bf16 at bytes 528 + 2 (c - 512).  Four group scales + kpe
+    scale: c < 512 -> e4m3 * k_scale[idx, c // 128]; c >= 512 -> e4m3 * kpe."""
+    import struct
+    w = W.custom(T=1, h=1, topk=1, num_slots=7, kv_dtype=kv_dtype, valid=[1],
+                 seed=18, k_scale=0.37)
+    idx = int(w.indices[0, 0])
+    row = bytes(w.kv[idx].numpy().tobytes())
+    for c in [0, 5, 127, 128, 255, 256, 300, 383, 384, 511, 512, 513, 543, 575]:
+        if kv_dtype == W.KV_FP8_DS_MLA:
+            if c < 512:
+                sc = struct.unpack("<f", row[512 + 4 * (c // 128): 516 + 4 * (c // 128)])[0]
+                val = _e4m3_torch(row[c]) * sc
+            else:
+                lo = 528 + 2 * (c - 512)
+                val = struct.unpack("<f", b"\x00\x00" + row[lo: lo + 2])[0]
+        else:
+            sc = float(w.k_scale[idx, c // 128]) if c < 512 else float(np.float32(0.37))
+            val = _e4m3_torch(row[c]) * sc
+        w.q.zero_()
+        w.q[0, 0, c] = 1.0
+        O, L = oracle_fwd(w)
+        _close(L[0, 0], w.sm_scale * val)
+        if c < 512:
+            _close(O[0, 0, c], val)
+
+
+def test_ds_mla_rows_equal_the_bf16_rows_they_encode():
+    """With power-of-two group scales every dequantized ckv value is a bf16
+    value, so a bf16 cache holding the same rows must give the same result
+    (both computed in fp64 from identical values)."""
+    S, T, h = 40, 3, 4
+    g = torch.Generator().manual_seed(5)
+    scales = 2.0 ** -torch.randint(2, 7, (S, 4), generator=g).float()
+    codes = W.fp8_cache_group(S, 512, scales, "cpu", g)
+    rope = W.bf16_normal((S, 64), "cpu", g)
+    ds = W.custom(T=T, h=h, topk=16, num_slots=S, kv_dtype=W.KV_FP8_DS_MLA,
+                  valid=[16, 9, 1], seed=6)
+    ds.kv = W.ds_mla_rows(codes, scales, rope)
+    bf = W.custom(T=T, h=h, topk=16, num_slots=S, valid=[16, 9, 1], seed=6)
+    ckv = codes.view(torch.float8_e4m3fn).to(torch.float32) * scales[:, torch.arange(512) // 128]
+    bf.kv = torch.cat([ckv.to(torch.bfloat16), rope], dim=1).contiguous()
+    assert torch.equal(bf.kv[:, :512].float(), ckv)          # the encoding is exact
+    bf.q, bf.indices, bf.valid_len = ds.q, ds.indices, ds.valid_len
+    O1, L1 = oracle_fwd(ds)
+    O2, L2 = oracle_fwd(bf)
+    assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
+
+
+def test_group4_kpe_equals_group128_with_the_kpe_scale_as_group_4():
+    """Four ckv group scales and a per-tensor kpe scale are the 5-group
+    layout whose fifth (rope) scale is that kpe scale for every slot."""
+    w4 = W.custom(T=3, h=3, topk=20, num_slots=50, kv_dtype=W.KV_FP8_E4M3_GROUP4_KPE,
+                  valid=[20, 7, 0], seed=9, k_scale=0.21)
+    w2 = W.custom(T=3, h=3, topk=20, num_slots=50, kv_dtype=W.KV_FP8_E4M3_GROUP128,
+                  valid=[20, 7, 0], seed=9)
+    w2.q, w2.kv, w2.indices, w2.valid_len = w4.q, w4.kv, w4.indices, w4.valid_len
+    w2.k_scale = torch.cat([w4.k_scale, torch.full((50, 1), 0.21)], dim=1).contiguous()
+    O1, L1 = oracle_fwd(w4)
+    O2, L2 = oracle_fwd(w2)
+    assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
+    assert np.isneginf(L1[2]).all()
