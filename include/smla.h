@@ -54,11 +54,24 @@ extern "C" {
  *  SMLA_KV_FP8_E4M3: E4M3 bytes, value = e4m3 * k_scale[0]
  *    (flashinfer_mla_sparse_sm90.py: per-tensor k_scale, FP8 read directly).
  *  SMLA_KV_FP8_E4M3_GROUP128: E4M3 bytes, value = e4m3 * k_scale[slot*G + c/128],
- *    G = ceil(d_qk/128) (the per-token x 128-channel-group ckv_scale_arr). */
+ *    G = ceil(d_qk/128) (the per-token x 128-channel-group ckv_scale_arr).
+ *  SMLA_KV_FP8_DS_MLA: d_qk = 576 only; 656-byte rows (the fp8_ds_mla cache
+ *    of vLLM "Sparse MLA on Hopper", cutlass_fa3_sparse.py module docstring:
+ *    656 bytes per token), read as bytes [0, 512) E4M3 ckv codes, [512, 528)
+ *    four little-endian fp32 scales (one per 128-channel group), [528, 656)
+ *    the 64 rope values as little-endian bf16; value = e4m3 * scale[c/128]
+ *    for c < 512, the bf16 rope value for c >= 512.  k_scale is unused.
+ *  SMLA_KV_FP8_E4M3_GROUP4_KPE: d_qk = 576 only; E4M3 bytes [num_slots, 576],
+ *    value = e4m3 * k_scale[slot*4 + c/128] for c < 512 and e4m3 * kpe_scale
+ *    for the 64 rope channels (the ckv_scale / kpe_scale split of
+ *    flashinfer_mla_sparse_sm90.py, forward_mqa).  Entry points without a
+ *    kpe_scale argument use 1.0, the value that page passes. */
 typedef enum {
   SMLA_KV_BF16 = 0,
   SMLA_KV_FP8_E4M3 = 1,
-  SMLA_KV_FP8_E4M3_GROUP128 = 2
+  SMLA_KV_FP8_E4M3_GROUP128 = 2,
+  SMLA_KV_FP8_DS_MLA = 3,
+  SMLA_KV_FP8_E4M3_GROUP4_KPE = 4
 } smla_kv_dtype;
 
 typedef enum {
@@ -79,10 +92,13 @@ typedef enum {
  *  q          device, bf16 [T, h, d_qk] contiguous; d_qk = 576 ([nope 512 |
  *             rope 64]) or 512 (NoPE).  16-byte aligned.
  *  kv_cache   device, [num_slots, d_qk] contiguous rows: bf16 (2*d_qk bytes a
- *             row) or E4M3 bytes (d_qk bytes a row).  16-byte aligned.
+ *             row) or E4M3 bytes (d_qk bytes a row); SMLA_KV_FP8_DS_MLA:
+ *             656-byte rows.  16-byte aligned.
  *  kv_dtype   an smla_kv_dtype value.
- *  k_scale    device fp32: NULL for SMLA_KV_BF16; [1] for SMLA_KV_FP8_E4M3;
- *             [num_slots, ceil(d_qk/128)] for SMLA_KV_FP8_E4M3_GROUP128.
+ *  k_scale    device fp32: NULL for SMLA_KV_BF16 and SMLA_KV_FP8_DS_MLA; [1]
+ *             for SMLA_KV_FP8_E4M3; [num_slots, ceil(d_qk/128)] for
+ *             SMLA_KV_FP8_E4M3_GROUP128; [num_slots, 4] for
+ *             SMLA_KV_FP8_E4M3_GROUP4_KPE.
  *  indices    device int32 [T, topk]: global slot ids; entries < 0 or
  *             >= num_slots are masked wherever they sit (the -1 tail, or
  *             scattered -1 as the flashmla_sparse page's DCP path leaves them).
@@ -312,6 +328,34 @@ SMLA_API const char* smla_status_string(int status);
 
 /* smla_version — library version as major*10000 + minor*100 + patch. */
 SMLA_API int smla_version(void);
+
+/*
+ * smla_fwd_split_q — smla_fwd with the query in two tensors and an explicit
+ * rope scale, as FlashInfer's run(q_nope, q_pe, ckv, kpe, ckv_scale,
+ * kpe_scale) and the FA3 sparse backend take them (flashinfer_mla_sparse_sm90.py,
+ * forward_mqa; vLLM "Sparse MLA on Hopper", cutlass_fa3_sparse.py module
+ * docstring: the two query parts go in separately, without a concatenation
+ * kernel).  The kernels read q_nope and q_pe where they sit.
+ *
+ *  q_nope     device, bf16 [T, h, 512] contiguous, 16-byte aligned; or, with
+ *             q_pe NULL, the concatenated q [T, h, d_qk] of smla_fwd.
+ *  q_pe       device, bf16 [T, h, d_qk - 512] contiguous, 16-byte aligned, or
+ *             NULL.  Ignored when d_qk = 512 (NoPE; the pages hand a
+ *             zero-width rope tensor through).
+ *  kpe_scale  the rope channels' scale for SMLA_KV_FP8_E4M3_GROUP4_KPE;
+ *             ignored by the other formats.
+ *  workspace, workspace_bytes  as smla_fwd_ws; workspace NULL = the
+ *             library-owned workspace of smla_fwd.
+ *  Every other argument, the results and the errors are those of smla_fwd.
+ */
+SMLA_API smla_status smla_fwd_split_q(const void* q_nope, const void* q_pe,
+                                      const void* kv_cache, int kv_dtype,
+                                      const float* k_scale, float kpe_scale,
+                                      const int32_t* indices, const int32_t* valid_len,
+                                      int T, int h, int d_qk, int d_v, int topk,
+                                      int64_t num_slots, float sm_scale, void* out,
+                                      float* lse, void* workspace, size_t workspace_bytes,
+                                      cudaStream_t stream);
 
 #ifdef __cplusplus
 }

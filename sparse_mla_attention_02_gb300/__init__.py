@@ -21,6 +21,9 @@ _lock = threading.Lock()
 SMLA_KV_BF16 = 0
 SMLA_KV_FP8_E4M3 = 1
 SMLA_KV_FP8_E4M3_GROUP128 = 2
+SMLA_KV_FP8_DS_MLA = 3            # 656-byte rows: 512 E4M3 | 4 fp32 scales | 64 bf16
+SMLA_KV_FP8_E4M3_GROUP4_KPE = 4   # E4M3 [S, 576], k_scale [S, 4], one kpe scale
+DS_MLA_ROW_BYTES = 656
 
 SMLA_OK = 0
 STATUS_NAMES = {0: "SMLA_OK", 1: "SMLA_ERR_INVALID_ARG",
@@ -65,6 +68,9 @@ def load():
         lib.smla_fwd_paged.argtypes = [P, P, I, P, P, P, P, I, I, I, I, P, I, I, I,
                                        I, I, I64, F, P, P, P, SZ, P]
         lib.smla_fwd_paged.restype = I
+        lib.smla_fwd_split_q.argtypes = [P, P, P, I, P, F, P, P, I, I, I, I, I, I64, F,
+                                         P, P, P, SZ, P]
+        lib.smla_fwd_split_q.restype = I
         lib.smla_workspace_size.argtypes = [I, I, I, I, I, I]
         lib.smla_workspace_size.restype = SZ
         lib.smla_plan_info.argtypes = [I, I, I, I, I, I, ctypes.POINTER(I),
@@ -98,25 +104,38 @@ def _check(code, what):
         raise SmlaError(code, what)
 
 
+def _kv_slots(kv_cache, kv_dtype, k_scale, d_qk, num_slots):
+    """Check the cache and its scales; return the slot count."""
+    import torch
+    assert kv_cache.is_cuda and kv_cache.is_contiguous()
+    if kv_dtype == SMLA_KV_BF16:
+        assert kv_cache.dtype == torch.bfloat16
+    else:
+        assert kv_cache.dtype == torch.uint8
+    if kv_dtype in (SMLA_KV_FP8_E4M3, SMLA_KV_FP8_E4M3_GROUP128, SMLA_KV_FP8_E4M3_GROUP4_KPE):
+        assert k_scale is not None and k_scale.dtype == torch.float32
+        assert k_scale.is_cuda and k_scale.is_contiguous()
+    row = DS_MLA_ROW_BYTES if kv_dtype == SMLA_KV_FP8_DS_MLA else d_qk
+    return kv_cache.numel() // row if num_slots is None else int(num_slots)
+
+
+def _idx_checks(indices, valid_len, T):
+    import torch
+    assert indices.is_cuda and indices.dtype == torch.int32
+    assert indices.is_contiguous() and indices.shape[0] == T
+    if valid_len is not None:
+        assert valid_len.is_cuda and valid_len.dtype == torch.int32
+        assert valid_len.is_contiguous() and valid_len.shape == (T,)
+
+
 def _in_args(q, kv_cache, kv_dtype, k_scale, indices, valid_len, sm_scale,
              num_slots):
     """The input arguments of the forward entry points, checked."""
     import torch
     assert q.is_cuda and q.dtype == torch.bfloat16 and q.is_contiguous()
     T, h, d_qk = q.shape
-    assert kv_cache.is_cuda and kv_cache.is_contiguous()
-    if kv_dtype == SMLA_KV_BF16:
-        assert kv_cache.dtype == torch.bfloat16
-    else:
-        assert kv_cache.dtype == torch.uint8
-        assert k_scale is not None and k_scale.dtype == torch.float32
-        assert k_scale.is_cuda and k_scale.is_contiguous()
-    S = kv_cache.numel() // d_qk if num_slots is None else int(num_slots)
-    assert indices.is_cuda and indices.dtype == torch.int32
-    assert indices.is_contiguous() and indices.shape[0] == T
-    if valid_len is not None:
-        assert valid_len.is_cuda and valid_len.dtype == torch.int32
-        assert valid_len.is_contiguous() and valid_len.shape == (T,)
+    S = _kv_slots(kv_cache, kv_dtype, k_scale, d_qk, num_slots)
+    _idx_checks(indices, valid_len, T)
     return [_p(q), _p(kv_cache), int(kv_dtype), _p(k_scale), _p(indices),
             _p(valid_len), T, h, d_qk, 512, indices.shape[1], S, float(sm_scale)]
 
@@ -126,20 +145,9 @@ def _fwd_args(q, kv_cache, kv_dtype, k_scale, indices, valid_len, sm_scale,
     import torch
     assert q.is_cuda and q.dtype == torch.bfloat16 and q.is_contiguous()
     T, h, d_qk = q.shape
-    assert kv_cache.is_cuda and kv_cache.is_contiguous()
-    if kv_dtype == SMLA_KV_BF16:
-        assert kv_cache.dtype == torch.bfloat16
-    else:
-        assert kv_cache.dtype == torch.uint8
-        assert k_scale is not None and k_scale.dtype == torch.float32
-        assert k_scale.is_cuda and k_scale.is_contiguous()
-    S = kv_cache.numel() // d_qk if num_slots is None else int(num_slots)
-    assert indices.is_cuda and indices.dtype == torch.int32
-    assert indices.is_contiguous() and indices.shape[0] == T
+    S = _kv_slots(kv_cache, kv_dtype, k_scale, d_qk, num_slots)
+    _idx_checks(indices, valid_len, T)
     topk = indices.shape[1]
-    if valid_len is not None:
-        assert valid_len.is_cuda and valid_len.dtype == torch.int32
-        assert valid_len.is_contiguous() and valid_len.shape == (T,)
     d_v = 512
     if out is None:
         out = torch.empty((T, h, d_v), dtype=torch.bfloat16, device=q.device)
@@ -168,6 +176,41 @@ def smla_fwd(q, kv_cache, kv_dtype, k_scale, indices, valid_len, sm_scale,
     args, out, lse = _fwd_args(q, kv_cache, kv_dtype, k_scale, indices,
                                valid_len, sm_scale, out, lse, num_slots)
     _check(lib.smla_fwd(*args, _stream(stream)), "smla_fwd")
+    return out, lse
+
+
+def smla_fwd_split_q(q_nope, q_pe, kv_cache, kv_dtype, k_scale, indices, valid_len,
+                     sm_scale, kpe_scale=1.0, out=None, lse=None, want_lse=True,
+                     num_slots=None, workspace=None, stream=None):
+    """``smla_fwd_split_q``: the forward on q_nope bf16 [T,h,512] and q_pe
+    bf16 [T,h,d_qk-512] (or None: q_nope is the concatenated q), with the
+    rope scale kpe_scale for SMLA_KV_FP8_E4M3_GROUP4_KPE.
+    Returns (out bf16 [T,h,512], lse f32 [T,h] or None)."""
+    import torch
+    lib = load()
+    assert q_nope.is_cuda and q_nope.dtype == torch.bfloat16 and q_nope.is_contiguous()
+    if q_pe is None:
+        T, h, d_qk = q_nope.shape
+    else:
+        T, h, d_nope = q_nope.shape
+        assert d_nope == 512 and q_pe.shape[:2] == (T, h)
+        assert q_pe.is_cuda and q_pe.dtype == torch.bfloat16 and q_pe.is_contiguous()
+        d_qk = 512 + q_pe.shape[2]
+    S = _kv_slots(kv_cache, kv_dtype, k_scale, d_qk, num_slots)
+    _idx_checks(indices, valid_len, T)
+    if out is None:
+        out = torch.empty((T, h, 512), dtype=torch.bfloat16, device=q_nope.device)
+    assert out.dtype == torch.bfloat16 and out.is_contiguous() and out.shape == (T, h, 512)
+    if lse is None and want_lse:
+        lse = torch.empty((T, h), dtype=torch.float32, device=q_nope.device)
+    if lse is not None:
+        assert lse.dtype == torch.float32 and lse.is_contiguous() and lse.shape == (T, h)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.smla_fwd_split_q(_p(q_nope), _p(q_pe), _p(kv_cache), int(kv_dtype),
+                                _p(k_scale), float(kpe_scale), _p(indices), _p(valid_len),
+                                T, h, d_qk, 512, indices.shape[1], S, float(sm_scale),
+                                _p(out), _p(lse), _p(workspace), nbytes, _stream(stream)),
+           "smla_fwd_split_q")
     return out, lse
 
 

@@ -65,11 +65,15 @@ smla_status check_args(const void* q, const void* kv, int kv_dtype,
   if (d_qk != 512 && d_qk != 576) return SMLA_ERR_UNSUPPORTED;
   if (d_v != 512) return SMLA_ERR_UNSUPPORTED;
   if (num_slots > 0x7FFFFFFFLL) return SMLA_ERR_UNSUPPORTED;
-  if (kv_dtype < SMLA_KV_BF16 || kv_dtype > SMLA_KV_FP8_E4M3_GROUP128)
+  if (kv_dtype < SMLA_KV_BF16 || kv_dtype > SMLA_KV_FP8_E4M3_GROUP4_KPE)
+    return SMLA_ERR_UNSUPPORTED;
+  if ((kv_dtype == SMLA_KV_FP8_DS_MLA || kv_dtype == SMLA_KV_FP8_E4M3_GROUP4_KPE) &&
+      d_qk != 576)
     return SMLA_ERR_UNSUPPORTED;
   if (T == 0) return SMLA_OK;
   if (!q || !kv || !indices || !out) return SMLA_ERR_INVALID_ARG;
-  if (kv_dtype != SMLA_KV_BF16 && !k_scale) return SMLA_ERR_INVALID_ARG;
+  if (kv_dtype != SMLA_KV_BF16 && kv_dtype != SMLA_KV_FP8_DS_MLA && !k_scale)
+    return SMLA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16) ||
       !aligned(indices, 4) || (k_scale && !aligned(k_scale, 4)))
     return SMLA_ERR_INVALID_ARG;
@@ -90,10 +94,13 @@ smla_status run_fwd(const void* q, const void* kv, int kv_dtype,
                     int topk, int64_t num_slots, float sm_scale, void* out,
                     float* lse, void* ws, size_t ws_bytes, bool own_ws,
                     cudaStream_t stream, const Paged& pg = Paged(),
-                    float* out_f32 = nullptr) {
+                    float* out_f32 = nullptr, const void* q_pe = nullptr,
+                    float kpe_scale = 1.0f) {
   smla_status st = check_args(q, kv, kv_dtype, k_scale, indices, T, h, d_qk,
                               d_v, topk, num_slots, out);
   if (st != SMLA_OK || T == 0) return st;
+  if (d_qk == 512) q_pe = nullptr;             // NoPE: no rope part to read
+  if (q_pe && !aligned(q_pe, 16)) return SMLA_ERR_INVALID_ARG;
   if (pg.table) {
     if (!pg.req_id || pg.num_reqs < 1 || pg.bt_stride < 1 || pg.block_size < 1 ||
         pg.stride_rows < 1 || !aligned(pg.req_id, 4) || !aligned(pg.table, 4) ||
@@ -140,8 +147,10 @@ smla_status run_fwd(const void* q, const void* kv, int kv_dtype,
   }
   smla::FwdParams p{};
   p.q = q;
+  p.q_pe = q_pe;
   p.kv = kv;
   p.k_scale = k_scale;
+  p.kpe_scale = kpe_scale;
   p.indices = indices;
   p.valid_len = valid_len;
   p.out = out;
@@ -324,6 +333,17 @@ smla_status smla_fwd_paged(const void* q, const void* kv_cache, int kv_dtype,
                  workspace_bytes, workspace == nullptr, stream, pg);
 }
 
+smla_status smla_fwd_split_q(const void* q_nope, const void* q_pe, const void* kv_cache,
+                             int kv_dtype, const float* k_scale, float kpe_scale,
+                             const int32_t* indices, const int32_t* valid_len, int T, int h,
+                             int d_qk, int d_v, int topk, int64_t num_slots, float sm_scale,
+                             void* out, float* lse, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream) {
+  return run_fwd(q_nope, kv_cache, kv_dtype, k_scale, indices, valid_len, T, h, d_qk, d_v,
+                 topk, num_slots, sm_scale, out, lse, workspace, workspace_bytes,
+                 workspace == nullptr, stream, Paged(), nullptr, q_pe, kpe_scale);
+}
+
 size_t smla_workspace_size(int T, int h, int d_qk, int d_v, int topk,
                            int kv_dtype) {
   if (T <= 0 || h < 1 || topk < 1) return 0;
@@ -341,7 +361,9 @@ smla_status smla_plan_info(int T, int h, int d_qk, int d_v, int topk,
                            size_t* workspace_bytes) {
   if (T < 1 || h < 1 || topk < 1) return SMLA_ERR_INVALID_ARG;
   if (h > 128 || (d_qk != 512 && d_qk != 576) || d_v != 512 ||
-      kv_dtype < SMLA_KV_BF16 || kv_dtype > SMLA_KV_FP8_E4M3_GROUP128)
+      kv_dtype < SMLA_KV_BF16 || kv_dtype > SMLA_KV_FP8_E4M3_GROUP4_KPE ||
+      ((kv_dtype == SMLA_KV_FP8_DS_MLA || kv_dtype == SMLA_KV_FP8_E4M3_GROUP4_KPE) &&
+       d_qk != 576))
     return SMLA_ERR_UNSUPPORTED;
   DeviceInfo* dev = nullptr;
   {

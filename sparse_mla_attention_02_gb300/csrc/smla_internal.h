@@ -9,16 +9,24 @@
 
 namespace smla {
 
-enum KvFormat { kBf16 = 0, kE4m3 = 1, kE4m3Group = 2 };
+// kDsMla: 656-byte rows [512 E4M3 | 4 fp32 group scales | 64 bf16 rope];
+// kE4m3Group4Kpe: E4M3 [num_slots, 576] with k_scale [num_slots, 4] for the
+// 512 ckv channels and one fp32 kpe_scale for the 64 rope channels.
+enum KvFormat { kBf16 = 0, kE4m3 = 1, kE4m3Group = 2, kDsMla = 3, kE4m3Group4Kpe = 4 };
+constexpr int kDsMlaRowBytes = 656;
+constexpr int kDsMlaScaleOff = 512;   // 4 fp32 scales
+constexpr int kDsMlaRopeOff = 528;    // 64 bf16 values
 
 // Bits of the device status word (first condition wins, see smla_api.cu).
 enum StatusBits { kStatusTimeout = 4, kStatusBadIndex = 5 };
 
 // Everything a forward launch needs.  Pointers are device pointers.
 struct FwdParams {
-  const void* q;          // bf16 [T, h, d_qk]
-  const void* kv;         // [num_slots, d_qk] bf16 or E4M3 bytes
-  const float* k_scale;   // per-tensor [1] or group [num_slots, G]
+  const void* q;          // bf16 [T, h, d_qk], or q_nope [T, h, 512] if q_pe
+  const void* q_pe;       // bf16 [T, h, d_qk - 512] or nullptr (q concatenated)
+  const void* kv;         // [num_slots, d_qk] bf16 or E4M3 bytes, or 656-byte rows
+  const float* k_scale;   // per-tensor [1], group [num_slots, G], [num_slots, 4]
+  float kpe_scale;        // rope scale of kE4m3Group4Kpe
   const int32_t* indices; // [T, topk]
   const int32_t* valid_len;  // [T] or nullptr
   void* out;              // bf16 [T, h, d_v]
@@ -44,6 +52,16 @@ struct FwdParams {
 };
 
 #ifdef __CUDACC__
+// Channels [ch, ch + 8) of q[t, hd] (ch a multiple of 8) as one 16-byte load.
+__device__ __forceinline__ const uint4* q_chunk(const FwdParams& p, int t, int hd, int ch) {
+  const int64_t row = (int64_t)t * p.h + hd;
+  const uint16_t* base =
+      !p.q_pe    ? static_cast<const uint16_t*>(p.q) + row * p.d_qk + ch
+      : ch < 512 ? static_cast<const uint16_t*>(p.q) + row * 512 + ch
+                 : static_cast<const uint16_t*>(p.q_pe) + row * (p.d_qk - 512) + (ch - 512);
+  return reinterpret_cast<const uint4*>(base);
+}
+
 // The global slot for top-k entry value `e` of a token whose request is
 // `req` (-1 when the token's request id is out of range): e itself for
 // global indices; the block-table translation for request-local ones.

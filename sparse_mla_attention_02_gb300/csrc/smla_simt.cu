@@ -9,7 +9,11 @@
 //       compacted valid prefix, -1 past it),
 //   a2  gathers the selected rows into shared memory (16-byte loads),
 //   a3  dequantizes E4M3 with the per-tensor or per-(slot, 128-channel group)
-//       scale (same page, module docstring),
+//       scale (same page, module docstring), the 656-byte fp8_ds_mla row
+//       (scales and bf16 rope inside the row; vLLM "Sparse MLA on Hopper",
+//       cutlass_fa3_sparse.py module docstring: 656 bytes per token), or four
+//       ckv group scales with a separate kpe scale (flashinfer page,
+//       forward_mqa: ckv_scale and kpe_scale),
 //   a4  forms s = sm_scale * q . K over d_qk (vLLM "Sparse MLA on Hopper",
 //       ops/cutlass_fa3.py docstring: score = q_rope.k_rope + q_nope.c_kv),
 //   a5  updates the running max / sum (online softmax),
@@ -87,10 +91,22 @@ smla_simt_kernel(FwdParams p, int n_groups) {
   const int k1 = min(k0 + p.split_len, v);
 
   // Q rows of this head group -> fp32 in shared memory (zero past nh).
-  const uint16_t* qg = reinterpret_cast<const uint16_t*>(p.q) +
-                       ((int64_t)t * p.h + h0) * d_qk;
-  for (int i = tid; i < kHeads * d_qk; i += kThreads)
-    Qs[i] = (i < nh * d_qk) ? bf16_bits_to_float(qg[i]) : 0.f;
+  for (int i = tid; i < kHeads * (d_qk / 8); i += kThreads) {
+    const int hh = i / (d_qk / 8), c = (i % (d_qk / 8)) * 8;
+    float* dst = Qs + hh * d_qk + c;
+    if (hh < nh) {
+      const uint4 w = __ldg(q_chunk(p, t, h0 + hh, c));
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        dst[2 * e] = bf16_bits_to_float(ws[e] & 0xFFFFu);
+        dst[2 * e + 1] = bf16_bits_to_float(ws[e] >> 16);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) dst[e] = 0.f;
+    }
+  }
   if (tid < kHeads) {
     m_s[tid] = -INFINITY;
     l_s[tid] = 0.f;
@@ -144,11 +160,28 @@ smla_simt_kernel(FwdParams p, int n_groups) {
         if (id < 0) {
 #pragma unroll
           for (int e = 0; e < 16; ++e) dst[e] = 0.f;
+        } else if (KV == kDsMla && c >= 512) {
+          // rope: 16 bf16 values (32 bytes) of the 656-byte row
+          const uint4* src = reinterpret_cast<const uint4*>(
+              reinterpret_cast<const uint8_t*>(p.kv) + (int64_t)id * kDsMlaRowBytes +
+              kDsMlaRopeOff + 2 * (c - 512));
+          const uint4 w0 = __ldg(src), w1 = __ldg(src + 1);
+          const uint32_t ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            dst[2 * e] = bf16_bits_to_float(ws[e] & 0xFFFFu);
+            dst[2 * e + 1] = bf16_bits_to_float(ws[e] >> 16);
+          }
         } else {
-          const uint4 w = *reinterpret_cast<const uint4*>(
-              reinterpret_cast<const uint8_t*>(p.kv) + (int64_t)id * d_qk + c);
-          const float sc = (KV == kE4m3) ? p.k_scale[0]
-                                         : p.k_scale[(int64_t)id * G + c / 128];
+          const uint8_t* row = reinterpret_cast<const uint8_t*>(p.kv) +
+                               (int64_t)id * (KV == kDsMla ? kDsMlaRowBytes : d_qk);
+          const uint4 w = __ldg(reinterpret_cast<const uint4*>(row + c));
+          float sc;
+          if (KV == kE4m3) sc = p.k_scale[0];
+          else if (KV == kE4m3Group) sc = p.k_scale[(int64_t)id * G + c / 128];
+          else if (KV == kDsMla)
+            sc = __ldg(reinterpret_cast<const float*>(row + kDsMlaScaleOff) + c / 128);
+          else sc = c < 512 ? p.k_scale[(int64_t)id * 4 + c / 128] : p.kpe_scale;
           const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
           for (int e = 0; e < 16; ++e)
@@ -273,33 +306,28 @@ size_t simt_smem_bytes(int d_qk) {
          sizeof(int) * kBlock;
 }
 
+template <int KV>
+cudaError_t launch_simt_fmt(const FwdParams& p, int n_groups, int64_t blocks, size_t smem,
+                            cudaStream_t stream) {
+  const cudaError_t e = cudaFuncSetAttribute(
+      smla_simt_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  smla_simt_kernel<KV><<<(unsigned)blocks, kThreads, smem, stream>>>(p, n_groups);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_simt(const FwdParams& p, cudaStream_t stream) {
   const int n_groups = (p.h + kHeads - 1) / kHeads;
   const int64_t blocks = (int64_t)p.T * n_groups * p.splits;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
   const size_t smem = simt_smem_bytes(p.d_qk);
-  cudaError_t e;
   switch (p.kv_format) {
-    case kBf16:
-      e = cudaFuncSetAttribute(smla_simt_kernel<kBf16>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      smla_simt_kernel<kBf16><<<(unsigned)blocks, kThreads, smem, stream>>>(p, n_groups);
-      break;
-    case kE4m3:
-      e = cudaFuncSetAttribute(smla_simt_kernel<kE4m3>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      smla_simt_kernel<kE4m3><<<(unsigned)blocks, kThreads, smem, stream>>>(p, n_groups);
-      break;
-    default:
-      e = cudaFuncSetAttribute(smla_simt_kernel<kE4m3Group>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      smla_simt_kernel<kE4m3Group><<<(unsigned)blocks, kThreads, smem, stream>>>(p, n_groups);
-      break;
+    case kBf16: return launch_simt_fmt<kBf16>(p, n_groups, blocks, smem, stream);
+    case kE4m3: return launch_simt_fmt<kE4m3>(p, n_groups, blocks, smem, stream);
+    case kE4m3Group: return launch_simt_fmt<kE4m3Group>(p, n_groups, blocks, smem, stream);
+    case kDsMla: return launch_simt_fmt<kDsMla>(p, n_groups, blocks, smem, stream);
+    default: return launch_simt_fmt<kE4m3Group4Kpe>(p, n_groups, blocks, smem, stream);
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const float* o_parts, const float* lse_parts,

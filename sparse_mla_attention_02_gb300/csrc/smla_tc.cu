@@ -368,15 +368,14 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
     // Q half -> TMEM (rows >= h are zero): 16-column groups [0, 5) by the
     // first warpgroup, [5, ksteps / 2) by the second.
     {
-      const uint4* qrow = reinterpret_cast<const uint4*>(
-          reinterpret_cast<const uint16_t*>(p.q) +
-          ((int64_t)t * p.h + (head < p.h ? head : 0)) * p.d_qk + a.q_lo[r]);
+      const int hq = head < p.h ? head : 0;
       const int g0 = wg == 0 ? 0 : 5, g1 = wg == 0 ? 5 : a.ksteps / 2;
       uint4 qv[20];
 #pragma unroll
       for (int c = 0; c < 20; ++c)
-        qv[c] = (head < p.h && c < 4 * (g1 - g0)) ? __ldg(qrow + 4 * g0 + c)
-                                                  : make_uint4(0u, 0u, 0u, 0u);
+        qv[c] = (head < p.h && c < 4 * (g1 - g0))
+                    ? __ldg(q_chunk(p, t, hq, a.q_lo[r] + 8 * (4 * g0 + c)))
+                    : make_uint4(0u, 0u, 0u, 0u);
       __syncwarp();
 #pragma unroll
       for (int k = 0; k < 5; ++k) {

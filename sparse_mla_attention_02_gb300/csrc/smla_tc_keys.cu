@@ -159,7 +159,8 @@ __device__ __forceinline__ float xreduce16(float (&v)[kN], int lane) {
 template <int kFmt>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
-  constexpr bool kGroup = kFmt == kE4m3Group;
+  // Formats with per-(slot, group) scales: one QK accumulator per group.
+  constexpr bool kGroup = kFmt == kE4m3Group || kFmt == kDsMla || kFmt == kE4m3Group4Kpe;
   constexpr bool kFp8 = kFmt != kBf16;
   // P^T buffers: group scales need 4 copies (2 groups x hi/lo) in one buffer;
   // otherwise one copy, double-buffered.
@@ -335,45 +336,66 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
       // One thread per key row; all 16-byte loads of the row are in flight
       // before the stage is awaited; then exact E4M3 -> bf16 conversion into
       // the 128-byte-swizzled tile.  Masked rows are zero.
+      // 656-byte rows: the rope is bf16 (four 16-byte pieces per CTA, copied
+      // as they are), the group scales sit in the row, the rope's is 1.
       const int row = tid - 32;
       const uint32_t sw = (uint32_t)row & 7u;
-      const int n_u = ksteps;                                // 16-byte pieces: 18 or 16
+      const bool rope = ksteps > 16;                         // d_qk 576
+      constexpr int kRope = kFmt == kDsMla ? 4 : 2;          // rope pieces
+      const int row_bytes = kFmt == kDsMla ? kDsMlaRowBytes : p.d_qk;
+      const uint32_t rope_off =
+          kFmt == kDsMla ? (uint32_t)(kDsMlaRopeOff + 64 * (int)r) : (uint32_t)rope_lo;
+      const int scale_stride = kFmt == kE4m3Group4Kpe ? 4 : a.G;
       const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
       for (int b = 0; b < nb; ++b) {
         const int s = b & 1;
         const int id = slots[b * kBK + row];
-        const uint8_t* rowp = kv8 + (size_t)(id < 0 ? 0 : id) * p.d_qk;
+        const uint8_t* rowp = kv8 + (size_t)(id < 0 ? 0 : id) * row_bytes;
         const uint4* src = reinterpret_cast<const uint4*>(rowp + g_lo);
-        const uint4* srope = reinterpret_cast<const uint4*>(rowp + rope_lo);
-        uint4 rw[18];
+        const uint4* srope = reinterpret_cast<const uint4*>(rowp + rope_off);
+        uint4 rw[16 + kRope];
 #pragma unroll
-        for (int u = 0; u < 18; ++u)
-          rw[u] = (id >= 0 && u < n_u) ? __ldg(u < 16 ? src + u : srope + (u - 16))
-                                       : make_uint4(0u, 0u, 0u, 0u);
+        for (int u = 0; u < 16 + kRope; ++u)
+          rw[u] = (id >= 0 && (u < 16 || rope)) ? __ldg(u < 16 ? src + u : srope + (u - 16))
+                                                : make_uint4(0u, 0u, 0u, 0u);
         if (b + 1 < nb) {
           // the row of the next block into L2 while this one is converted
           const int idn = slots[(b + 1) * kBK + row];
           if (idn >= 0) {
-            const uint8_t* rn = kv8 + (size_t)idn * p.d_qk;
+            const uint8_t* rn = kv8 + (size_t)idn * row_bytes;
             prefetch_l2(rn + g_lo);
             prefetch_l2(rn + g_lo + 128);
             prefetch_l2(rn + g_lo + 255);
-            if (n_u > 16) prefetch_l2(rn + rope_lo);
-            if (kGroup) prefetch_l2(p.k_scale + (int64_t)idn * a.G);
+            if (rope) prefetch_l2(rn + rope_off);
+            if (kFmt == kDsMla) {
+              prefetch_l2(rn + kDsMlaScaleOff);
+              prefetch_l2(rn + rope_off + 63);
+            } else if (kGroup) {
+              prefetch_l2(p.k_scale + (int64_t)idn * scale_stride);
+            }
           }
         }
         float sc[3] = {0.f, 0.f, 0.f};
         if (kGroup && id >= 0) {
-          const float* srow = p.k_scale + (int64_t)id * a.G;
+          const float* srow = kFmt == kDsMla
+                                  ? reinterpret_cast<const float*>(rowp + kDsMlaScaleOff)
+                                  : p.k_scale + (int64_t)id * scale_stride;
           sc[0] = __ldg(srow + 2 * (int)r);
           sc[1] = __ldg(srow + 2 * (int)r + 1);
-          if (n_lg > 2) sc[2] = __ldg(srow + 4);
+          if (n_lg > 2)
+            sc[2] = kFmt == kE4m3Group ? __ldg(srow + 4) : kFmt == kDsMla ? 1.f : p.kpe_scale;
         }
         if (b >= kStages) W.wait(bar(kBarKvEmpty + s), ((b >> 1) - 1) & 1);
         uint8_t* rgen = sm + kOffTile + s * kStageBytes + row * 128;
 #pragma unroll
-        for (int u = 0; u < 18; ++u) {
-          if (u < n_u) {
+        for (int u = 0; u < 16 + kRope; ++u) {
+          if (kFmt == kDsMla && u >= 16) {
+            if (rope) {                                     // bf16 piece, as is
+              const uint32_t cj = 16u + (uint32_t)u;        // chunks 32..35
+              *reinterpret_cast<uint4*>(rgen + (cj >> 3) * kChunkBytes +
+                                        (((cj & 7u) ^ sw) << 4)) = rw[u];
+            }
+          } else if (u < 16 || rope) {
             uint32_t o[8];
             e4m3x4_to_bf16(rw[u].x, o[0], o[1]);
             e4m3x4_to_bf16(rw[u].y, o[2], o[3]);
@@ -436,16 +458,14 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
     {
       const int per_head = 2 * ksteps;                   // 16-byte pieces per head
       const int total = kN * per_head;                   // <= 576
-      const uint4* q4 = reinterpret_cast<const uint4*>(p.q);
       uint4 qv[5];
 #pragma unroll
       for (int k = 0; k < 5; ++k) {
         const int idx = i + kSoftmax * k;
         const int hd = idx / per_head, c16 = idx - hd * per_head;
         const int ch = c16 < 32 ? g_lo + 8 * c16 : rope_lo + 8 * (c16 - 32);
-        qv[k] = (idx < total && hd < p.h)
-                    ? __ldg(q4 + (((int64_t)t * p.h + hd) * p.d_qk + ch) / 8)
-                    : make_uint4(0u, 0u, 0u, 0u);
+        qv[k] = (idx < total && hd < p.h) ? __ldg(q_chunk(p, t, hd, ch))
+                                          : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
       for (int k = 0; k < 5; ++k) {
@@ -735,8 +755,9 @@ cudaError_t launch_keys(const KeysArgs& a, unsigned blocks, cudaStream_t stream)
 int tc_keys_max_range() { return kMaxBlocks * kBK; }
 
 bool tc_keys_supported(int h, int d_qk, int kv_format) {
-  return h >= 1 && h <= kN && (d_qk == 576 || d_qk == 512) &&
-         (kv_format == kBf16 || kv_format == kE4m3 || kv_format == kE4m3Group);
+  if (h < 1 || h > kN || (d_qk != 576 && d_qk != 512)) return false;
+  if (kv_format == kDsMla || kv_format == kE4m3Group4Kpe) return d_qk == 576;
+  return kv_format == kBf16 || kv_format == kE4m3 || kv_format == kE4m3Group;
 }
 
 cudaError_t launch_tc_keys(const FwdParams& p, cudaStream_t stream) {
@@ -755,7 +776,9 @@ cudaError_t launch_tc_keys(const FwdParams& p, cudaStream_t stream) {
   switch (p.kv_format) {
     case kBf16: return launch_keys<kBf16>(a, blocks, stream);
     case kE4m3: return launch_keys<kE4m3>(a, blocks, stream);
-    default:    return launch_keys<kE4m3Group>(a, blocks, stream);
+    case kE4m3Group: return launch_keys<kE4m3Group>(a, blocks, stream);
+    case kDsMla: return launch_keys<kDsMla>(a, blocks, stream);
+    default:    return launch_keys<kE4m3Group4Kpe>(a, blocks, stream);
   }
 }
 

@@ -59,7 +59,9 @@ def _fwd(lib, **kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(T=-1), 1), (dict(h=0), 1), (dict(topk=0), 1), (dict(S=0), 1),
     (dict(h=129), 2), (dict(d_qk=128), 2), (dict(d_v=256), 2),
-    (dict(kv_dtype=3), 2), (dict(S=1 << 31), 2),
+    (dict(kv_dtype=5), 2), (dict(kv_dtype=-1), 2), (dict(S=1 << 31), 2),
+    (dict(kv_dtype=3, d_qk=512), 2), (dict(kv_dtype=4, d_qk=512), 2),
+    (dict(kv_dtype=4), 1),
     (dict(q=None), 1), (dict(kv=None), 1), (dict(idx=None), 1),
     (dict(out=None), 1), (dict(kv_dtype=1), 1), (dict(kv_dtype=2), 1),
     (dict(q=(1 << 12) + 8), 1), (dict(out=(1 << 12) + 4), 1),
@@ -101,7 +103,9 @@ def test_plan_info_argument_checks(lib):
     assert q(4, 129, 576, 512, 64, 0) == 2
     assert q(4, 16, 640, 512, 64, 0) == 2
     assert q(4, 16, 576, 256, 64, 0) == 2
-    assert q(4, 16, 576, 512, 64, 3) == 2
+    assert q(4, 16, 576, 512, 64, 5) == 2
+    assert q(4, 16, 512, 512, 64, 3) == 2     # the 656-byte row is 576 channels
+    assert q(4, 16, 512, 512, 64, 4) == 2
     assert k.value == -1                      # outputs untouched on error
 
 
@@ -166,3 +170,18 @@ def test_cache_write_argument_checks(lib):
     assert f(d=512) == 1                 # 512-channel rows take no k_pe
     assert f(kv=4104) == 1               # misaligned
     assert f(c=4104) == 1
+
+
+def test_split_q_argument_checks(lib):
+    P = ctypes.c_void_p
+    f = lambda qn=4096, qp=4096, kv_dtype=0, ks=None, d_qk=576, T=4: lib.smla_fwd_split_q(
+        None if qn is None else P(qn), None if qp is None else P(qp), P(4096), kv_dtype,
+        None if ks is None else P(ks), 0.5, P(4096), None, T, 16, d_qk, 512, 64, 256, 0.04,
+        P(4096), None, None, 0, None)
+    assert f(qn=None) == 1
+    assert f(qp=4104) == 1                    # q_pe not 16-byte aligned
+    assert f(qn=4104) == 1
+    assert f(kv_dtype=4) == 1                 # four group scales needed
+    assert f(kv_dtype=3, d_qk=512) == 2
+    assert f(kv_dtype=5) == 2
+    assert f(T=0, qn=None, qp=None) == 0
