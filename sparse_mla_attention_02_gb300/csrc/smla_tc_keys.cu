@@ -46,7 +46,8 @@
 //
 // Warp roles (352 threads): warp 0 issues the QK MMAs and owns TMEM; warp 10
 // issues the PV MMAs; warps 1..4 load the unit's slot ids, then gather
-// (bf16: TMA; E4M3: one thread per key row loads, converts and stores);
+// (bf16: TMA; E4M3: each warp loads 32 rows cooperatively, 16 lanes a row,
+// and converts and stores what it loaded);
 // warp 5 tells the peer when its partial scores were consumed; warps 6..9
 // (thread <-> key <-> TMEM lane) load Q, run the exchange, softmax, O
 // rescale and the epilogue.  (Eleven warps leave each thread up to 168
@@ -333,34 +334,52 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
   } else if (warp <= 4) {
     // ---- loaders: a2 gather (+ a3 E4M3 conversion) -------------------------
     if (kFp8) {
-      // One thread per key row; all 16-byte loads of the row are in flight
-      // before the stage is awaited; then exact E4M3 -> bf16 conversion into
-      // the 128-byte-swizzled tile.  Masked rows are zero.
-      // 656-byte rows: the rope is bf16 (four 16-byte pieces per CTA, copied
-      // as they are), the group scales sit in the row, the rope's is 1.
-      const int row = tid - 32;
-      const uint32_t sw = (uint32_t)row & 7u;
-      const bool rope = ksteps > 16;                         // d_qk 576
-      constexpr int kRope = kFmt == kDsMla ? 4 : 2;          // rope pieces
+      // Warp-cooperative gather: loader warp w owns rows [32w, 32w + 32) of
+      // every block.  A row's 256 ckv bytes are read by 16 lanes, 16 bytes
+      // each, two rows per load instruction, so one instruction touches a few
+      // cache lines rather than 32; the rope pieces follow, 16 (E4M3) or 8
+      // (bf16) rows per instruction.  All loads of a block are in flight
+      // before the stage is awaited; then each lane converts what it loaded
+      // (exact E4M3 -> bf16) into the 128-byte-swizzled tile.  Masked rows
+      // are zero.  656-byte rows: the rope is bf16 (copied as it is), the
+      // group scales sit in the row, and the rope group's scale is 1.
+      const int w0 = (warp - 1) * 32;                      // the warp's first row
+      const int half = lane >> 4, pc = lane & 15;          // ckv: row of the pair, piece
+      const bool rope = ksteps > 16;                       // d_qk 576
+      constexpr int kRopeLanes = kFmt == kDsMla ? 4 : 2;   // 16-byte rope pieces a row
+      constexpr int kRopeRows = 32 / kRopeLanes;           // rows per rope instruction
+      constexpr int kRopeIns = 32 / kRopeRows;             // rope instructions per block
+      const int rpc = lane % kRopeLanes, rrow = lane / kRopeLanes;
       const int row_bytes = kFmt == kDsMla ? kDsMlaRowBytes : p.d_qk;
       const uint32_t rope_off =
           kFmt == kDsMla ? (uint32_t)(kDsMlaRopeOff + 64 * (int)r) : (uint32_t)rope_lo;
       const int scale_stride = kFmt == kE4m3Group4Kpe ? 4 : a.G;
       const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
+      const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
       for (int b = 0; b < nb; ++b) {
         const int s = b & 1;
-        const int id = slots[b * kBK + row];
-        const uint8_t* rowp = kv8 + (size_t)(id < 0 ? 0 : id) * row_bytes;
-        const uint4* src = reinterpret_cast<const uint4*>(rowp + g_lo);
-        const uint4* srope = reinterpret_cast<const uint4*>(rowp + rope_off);
-        uint4 rw[16 + kRope];
+        const int* bs = slots + b * kBK + w0;
+        uint4 ck[16], rq[kRopeIns];
 #pragma unroll
-        for (int u = 0; u < 16 + kRope; ++u)
-          rw[u] = (id >= 0 && (u < 16 || rope)) ? __ldg(u < 16 ? src + u : srope + (u - 16))
-                                                : make_uint4(0u, 0u, 0u, 0u);
+        for (int i = 0; i < 16; ++i) {
+          const int id = bs[2 * i + half];
+          ck[i] = id >= 0 ? __ldg(reinterpret_cast<const uint4*>(
+                                      kv8 + (size_t)id * row_bytes + g_lo) + pc)
+                          : zero4;
+        }
+#pragma unroll
+        for (int j = 0; j < kRopeIns; ++j) {
+          const int id = bs[kRopeRows * j + rrow];
+          rq[j] = (rope && id >= 0) ? __ldg(reinterpret_cast<const uint4*>(
+                                                kv8 + (size_t)id * row_bytes + rope_off) + rpc)
+                                    : zero4;
+        }
+        // The lane's own row (w0 + lane): its group scales, and the row of
+        // the next block into L2 while this one is converted.
+        const int id = bs[lane];
+        const uint8_t* rowp = kv8 + (size_t)(id < 0 ? 0 : id) * row_bytes;
         if (b + 1 < nb) {
-          // the row of the next block into L2 while this one is converted
-          const int idn = slots[(b + 1) * kBK + row];
+          const int idn = slots[(b + 1) * kBK + w0 + lane];
           if (idn >= 0) {
             const uint8_t* rn = kv8 + (size_t)idn * row_bytes;
             prefetch_l2(rn + g_lo);
@@ -386,31 +405,42 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
             sc[2] = kFmt == kE4m3Group ? __ldg(srow + 4) : kFmt == kDsMla ? 1.f : p.kpe_scale;
         }
         if (b >= kStages) W.wait(bar(kBarKvEmpty + s), ((b >> 1) - 1) & 1);
-        uint8_t* rgen = sm + kOffTile + s * kStageBytes + row * 128;
+        uint8_t* tile = sm + kOffTile + s * kStageBytes;
+        // 16-byte unit cj (8 bf16 channels) of `row` in the swizzled tile
+        auto unit = [&](int row, uint32_t cj) -> uint4* {
+          return reinterpret_cast<uint4*>(tile + row * 128 + (cj >> 3) * kChunkBytes +
+                                          (((cj & 7u) ^ ((uint32_t)row & 7u)) << 4));
+        };
 #pragma unroll
-        for (int u = 0; u < 16 + kRope; ++u) {
-          if (kFmt == kDsMla && u >= 16) {
-            if (rope) {                                     // bf16 piece, as is
-              const uint32_t cj = 16u + (uint32_t)u;        // chunks 32..35
-              *reinterpret_cast<uint4*>(rgen + (cj >> 3) * kChunkBytes +
-                                        (((cj & 7u) ^ sw) << 4)) = rw[u];
+        for (int i = 0; i < 16; ++i) {
+          const int row = w0 + 2 * i + half;
+          uint32_t o[8];
+          e4m3x4_to_bf16(ck[i].x, o[0], o[1]);
+          e4m3x4_to_bf16(ck[i].y, o[2], o[3]);
+          e4m3x4_to_bf16(ck[i].z, o[4], o[5]);
+          e4m3x4_to_bf16(ck[i].w, o[6], o[7]);
+          *unit(row, 2u * (uint32_t)pc) = make_uint4(o[0], o[1], o[2], o[3]);
+          *unit(row, 2u * (uint32_t)pc + 1u) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        if (rope) {
+#pragma unroll
+          for (int j = 0; j < kRopeIns; ++j) {
+            const int row = w0 + kRopeRows * j + rrow;
+            if (kFmt == kDsMla) {
+              *unit(row, 32u + (uint32_t)rpc) = rq[j];       // bf16, as is
+            } else {
+              uint32_t o[8];
+              e4m3x4_to_bf16(rq[j].x, o[0], o[1]);
+              e4m3x4_to_bf16(rq[j].y, o[2], o[3]);
+              e4m3x4_to_bf16(rq[j].z, o[4], o[5]);
+              e4m3x4_to_bf16(rq[j].w, o[6], o[7]);
+              *unit(row, 32u + 2u * (uint32_t)rpc) = make_uint4(o[0], o[1], o[2], o[3]);
+              *unit(row, 33u + 2u * (uint32_t)rpc) = make_uint4(o[4], o[5], o[6], o[7]);
             }
-          } else if (u < 16 || rope) {
-            uint32_t o[8];
-            e4m3x4_to_bf16(rw[u].x, o[0], o[1]);
-            e4m3x4_to_bf16(rw[u].y, o[2], o[3]);
-            e4m3x4_to_bf16(rw[u].z, o[4], o[5]);
-            e4m3x4_to_bf16(rw[u].w, o[6], o[7]);
-            const uint32_t cj = 2u * (uint32_t)u;               // two bf16 chunks
-            *reinterpret_cast<uint4*>(rgen + (cj >> 3) * kChunkBytes + (((cj & 7u) ^ sw) << 4)) =
-                make_uint4(o[0], o[1], o[2], o[3]);
-            const uint32_t cj1 = cj + 1u;
-            *reinterpret_cast<uint4*>(rgen + (cj1 >> 3) * kChunkBytes + (((cj1 & 7u) ^ sw) << 4)) =
-                make_uint4(o[4], o[5], o[6], o[7]);
           }
         }
         if (kGroup)
-          *reinterpret_cast<float4*>(sm + kOffScale + s * kScaleBytes + row * 16) =
+          *reinterpret_cast<float4*>(sm + kOffScale + s * kScaleBytes + (w0 + lane) * 16) =
               make_float4(sc[0], sc[1], sc[2], 0.f);
         fence_proxy_async_smem();
         mbar_arrive(bar(kBarKvFull + s));
