@@ -415,10 +415,10 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
         for (int i = 0; i < 16; ++i) {
           const int row = w0 + 2 * i + half;
           uint32_t o[8];
-          e4m3x4_to_bf16(ck[i].x, o[0], o[1]);
-          e4m3x4_to_bf16(ck[i].y, o[2], o[3]);
-          e4m3x4_to_bf16(ck[i].z, o[4], o[5]);
-          e4m3x4_to_bf16(ck[i].w, o[6], o[7]);
+          e4m3x4_to_bf16_sx(ck[i].x, o[0], o[1]);
+          e4m3x4_to_bf16_sx(ck[i].y, o[2], o[3]);
+          e4m3x4_to_bf16_sx(ck[i].z, o[4], o[5]);
+          e4m3x4_to_bf16_sx(ck[i].w, o[6], o[7]);
           *unit(row, 2u * (uint32_t)pc) = make_uint4(o[0], o[1], o[2], o[3]);
           *unit(row, 2u * (uint32_t)pc + 1u) = make_uint4(o[4], o[5], o[6], o[7]);
         }
@@ -430,10 +430,10 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
               *unit(row, 32u + (uint32_t)rpc) = rq[j];       // bf16, as is
             } else {
               uint32_t o[8];
-              e4m3x4_to_bf16(rq[j].x, o[0], o[1]);
-              e4m3x4_to_bf16(rq[j].y, o[2], o[3]);
-              e4m3x4_to_bf16(rq[j].z, o[4], o[5]);
-              e4m3x4_to_bf16(rq[j].w, o[6], o[7]);
+              e4m3x4_to_bf16_sx(rq[j].x, o[0], o[1]);
+              e4m3x4_to_bf16_sx(rq[j].y, o[2], o[3]);
+              e4m3x4_to_bf16_sx(rq[j].z, o[4], o[5]);
+              e4m3x4_to_bf16_sx(rq[j].w, o[6], o[7]);
               *unit(row, 32u + 2u * (uint32_t)rpc) = make_uint4(o[0], o[1], o[2], o[3]);
               *unit(row, 33u + 2u * (uint32_t)rpc) = make_uint4(o[4], o[5], o[6], o[7]);
             }
