@@ -276,7 +276,8 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
     const int g_lo = a.g_lo[r];
     if (a.fp8) {
       // a2 + a3 for an E4M3 cache: two threads per row load the row's bytes
-      // with 16-byte loads (all loads of a block in flight at once), convert
+      // with 16-byte loads (all loads of a block in flight at once, issued
+      // before the stage is free), convert
       // them exactly to bf16 and store the 128-byte-swizzled tile; masked
       // rows are zero.  The per-tensor scale is applied in fp32 later (score
       // scale and output normalization), so the tile holds exact values.
@@ -285,9 +286,19 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
       const uint32_t sw = (uint32_t)row & 7u;
       const int nc8 = a.n_chunks8[r];                         // <= 20
       const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
+      // The row of block j into L2 (the two threads of a row cover its up to
+      // four 128-byte lines); rows are prefetched two blocks ahead.
+      auto prefetch_row = [&](int j) {
+        const int idp = slots[j * kBN + row];
+        if (idp < 0) return;
+        const uint8_t* rp = kv8 + (size_t)idp * p.d_qk + g_lo;
+        prefetch_l2(rp + 128 * half);
+        prefetch_l2(rp + (half ? 16 * nc8 - 1 : min(256, 16 * nc8 - 1)));
+      };
+      if (nb > 1) prefetch_row(1);
       for (int b = 0; b < nb; ++b) {
         const int s = b % kStages;
-        if (b >= kStages) W.wait(bar(kBarKvEmpty + s), ((b / kStages) - 1) & 1);
+        if (b + 2 < nb) prefetch_row(b + 2);
         const int id = slots[b * kBN + row];
         const uint4* src = reinterpret_cast<const uint4*>(
             kv8 + (size_t)(id < 0 ? 0 : id) * p.d_qk + g_lo);
@@ -297,6 +308,8 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
           const int c = half + 2 * kk;
           raw[kk] = (id >= 0 && c < nc8) ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
         }
+        // The loads are in flight while the stage is awaited.
+        if (b >= kStages) W.wait(bar(kBarKvEmpty + s), ((b / kStages) - 1) & 1);
         uint8_t* rgen = sm + kOffTile + s * kTileBytes + row * 128;
 #pragma unroll
         for (int kk = 0; kk < 10; ++kk) {
