@@ -259,7 +259,7 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
     // tracks the MMAs of the issuing thread).
     if (nb > 0) {
       const uint32_t id_qk = idesc_bf16(128, kN, false, false);
-      const uint32_t id_pv = idesc_bf16(128, kNpv, true, false);
+      const uint32_t id_pv = idesc_bf16(128, kNpv, true, kGroup);
       const uint32_t qb = sb + kOffQ;
       auto issue_qk = [&](int j) {
         const int s = j & 1;
@@ -300,18 +300,22 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
         if (elect_one()) {
           fence_proxy_async_smem();
           // A = V^T: 128 channels (two 64-channel chunks) x 16 keys, MN-major;
-          // B = P^T of this channel group: 16 keys x N, K-major (group
-          // scales: rows 0..15 = hi, 16..31 = lo).
+          // B = P^T of this channel group: 16 keys x N.  Without group
+          // scales K-major (16 head rows of 128 keys); with them MN-major,
+          // one 128-byte row per key holding [g0 hi | g0 lo | g1 hi | g1 lo]
+          // (16 heads each), so group mb starts 64 mb bytes into the row.
           const uint64_t a0 = sdesc(tile, kChunkBytes, 1024, kLayoutSw128);
-          const uint64_t b0 = sdesc(pb, 16, 1024, kLayoutSw128);
+          const uint64_t b0 = kGroup ? sdesc(pb, kPAreaBytes, 1024, kLayoutSw128)
+                                     : sdesc(pb, 16, 1024, kLayoutSw128);
           const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
           for (int mb = 0; mb < 2; ++mb) {
 #pragma unroll
             for (int ks = 0; ks < kBK / 16; ++ks) {
               const uint32_t oa = (uint32_t)(2 * mb * kChunkBytes + ks * 16 * 128);
-              const uint32_t ob = (uint32_t)((kGroup ? mb * 2 * kPAtomBytes : 0) +
-                                             (ks >> 2) * kPAtomBytes + (ks & 3) * 32);
+              const uint32_t ob =
+                  kGroup ? (uint32_t)(64 * mb + ks * 16 * 128)
+                         : (uint32_t)((ks >> 2) * kPAtomBytes + (ks & 3) * 32);
               mma_ss(tmem + kColO + 2 * kN * mb, a0 + (oa >> 4), b0 + (ob >> 4), id_pv,
                      ks > 0 ? 1u : acc0);
             }
@@ -520,10 +524,14 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
     const uint32_t xrow = (uint32_t)i * kN * 4;          // this key's 64-byte row
     const uint32_t xsw = ((uint32_t)i >> 1) & 3u;        // its chunk swizzle
     float* red = reinterpret_cast<float*>(sm + kOffRed); // [16 heads][4 warps]
-    // This key's byte offset inside a P^T copy (K-major, 128-byte swizzle):
-    // K-atom (i / 64), 16-byte chunk ((i % 64) / 8) ^ (head % 8), element i % 8.
+    // Without group scales, this key's byte offset inside the K-major P^T
+    // (128-byte swizzle): K-atom (i / 64), 16-byte chunk ((i % 64) / 8) ^
+    // (head % 8), element i % 8.  With them, this key's 128-byte row of the
+    // MN-major P^T: atom i / 8, row i % 8, 16-byte chunk c at c ^ (i % 8).
     const uint32_t p_atom = (uint32_t)(i >> 6) * kPAtomBytes + (uint32_t)(i & 7) * 2u;
     const uint32_t p_chunk = (uint32_t)(i & 63) >> 3;
+    const uint32_t p_row = (uint32_t)(i >> 3) * 1024u + (uint32_t)(i & 7) * 128u;
+    const uint32_t p_sw = (uint32_t)(i & 7);
 
     for (int b = 0; b < nb; ++b) {
       const int s = b & 1;
@@ -545,17 +553,19 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
               *reinterpret_cast<const float4*>(sm + kOffScale + s * kScaleBytes + i * 16);
           scp0 = sc.x;
           scp1 = sc.y;
-          const float scl[3] = {sc.x, sc.y, sc.z};
+          // The group accumulators' loads are issued together, then awaited.
+          uint32_t w1[16], w2[16];
+          const uint32_t sc0 = tmem + lane_base + kColS + kSBuf * s;
+          tmem_ld16(sc0, w);
+          tmem_ld16(sc0 + kN, w1);
+          if (n_lg > 2) tmem_ld16(sc0 + 2 * kN, w2);   // same for every lane
+          tmem_wait_ld();
 #pragma unroll
-          for (int lg = 0; lg < 3; ++lg) {
-            if (lg < n_lg) {                 // same for every lane of the CTA
-              tmem_ld16(tmem + lane_base + kColS + kSBuf * s + kN * lg, w);
-              tmem_wait_ld();
+          for (int hd = 0; hd < kN; ++hd)
+            sp[hd] = fmaf(sc.y, __uint_as_float(w1[hd]), sc.x * __uint_as_float(w[hd]));
+          if (n_lg > 2) {
 #pragma unroll
-              for (int hd = 0; hd < kN; ++hd)
-                sp[hd] = lg == 0 ? scl[0] * __uint_as_float(w[hd])
-                                 : fmaf(scl[lg], __uint_as_float(w[hd]), sp[hd]);
-            }
+            for (int hd = 0; hd < kN; ++hd) sp[hd] = fmaf(sc.z, __uint_as_float(w2[hd]), sp[hd]);
           }
         } else {
           tmem_ld16(tmem + lane_base + kColS + kSBuf * s, w);
@@ -634,25 +644,38 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
       // each PV group as a bf16 pair hi + lo).
       const int pbi = b % kPBufs;
       if (b >= kPBufs) W.wait(bar(kBarPEmpty + pbi), ((b / kPBufs) - 1) & 1);  // PV read it
-      {
+      if (kGroup) {
+        // p * (group scale) = hi + lo, each bf16 (lo = the rounding error of
+        // hi); the key's row is written as eight 16-byte chunks.
+        uint8_t* prow = sm + kOffP + p_row;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          const float scg = g ? scp1 : scp0;
+          uint32_t hi[8], lo[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float v0 = pe[2 * k] * scg, v1 = pe[2 * k + 1] * scg;
+            hi[k] = pack_bf16(v0, v1);
+            lo[k] = pack_bf16(v0 - __uint_as_float(hi[k] << 16),
+                              v1 - __uint_as_float(hi[k] & 0xFFFF0000u));
+          }
+          const uint32_t c0 = 4u * (uint32_t)g;
+          *reinterpret_cast<uint4*>(prow + ((c0 ^ p_sw) << 4)) =
+              make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(prow + (((c0 + 1u) ^ p_sw) << 4)) =
+              make_uint4(hi[4], hi[5], hi[6], hi[7]);
+          *reinterpret_cast<uint4*>(prow + (((c0 + 2u) ^ p_sw) << 4)) =
+              make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          *reinterpret_cast<uint4*>(prow + (((c0 + 3u) ^ p_sw) << 4)) =
+              make_uint4(lo[4], lo[5], lo[6], lo[7]);
+        }
+      } else {
         uint8_t* pb = sm + kOffP + pbi * kPBufBytes + p_atom;
 #pragma unroll
         for (int hd = 0; hd < kN; ++hd) {
           const uint32_t off = (uint32_t)(hd >> 3) * 1024u + (uint32_t)(hd & 7) * 128u +
                                ((p_chunk ^ (uint32_t)(hd & 7)) << 4);
-          if (kGroup) {
-            // group g at g * 2 atoms; row hd = hi, row 16 + hd = lo (+2048 B)
-            const float v0 = pe[hd] * scp0, v1 = pe[hd] * scp1;
-            const __nv_bfloat16 h0 = __float2bfloat16_rn(v0), h1 = __float2bfloat16_rn(v1);
-            *reinterpret_cast<__nv_bfloat16*>(pb + off) = h0;
-            *reinterpret_cast<__nv_bfloat16*>(pb + 2048 + off) =
-                __float2bfloat16_rn(v0 - __bfloat162float(h0));
-            *reinterpret_cast<__nv_bfloat16*>(pb + 2 * kPAtomBytes + off) = h1;
-            *reinterpret_cast<__nv_bfloat16*>(pb + 2 * kPAtomBytes + 2048 + off) =
-                __float2bfloat16_rn(v1 - __bfloat162float(h1));
-          } else {
-            *reinterpret_cast<__nv_bfloat16*>(pb + off) = __float2bfloat16_rn(pe[hd]);
-          }
+          *reinterpret_cast<__nv_bfloat16*>(pb + off) = __float2bfloat16_rn(pe[hd]);
         }
       }
       fence_proxy_async_smem();
