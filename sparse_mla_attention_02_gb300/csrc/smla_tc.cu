@@ -496,14 +496,23 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
         sp[4 * c] += x.x; sp[4 * c + 1] += x.y; sp[4 * c + 2] += x.z; sp[4 * c + 3] += x.w;
       }
       mbar_arrive(bar(kBarXCons + buf));   // the signal warp tells the peer
-      // a5: masked online softmax (log2 domain).
+      // a5: masked online softmax (log2 domain).  When every position of
+      // this half-block is valid (and the scale is positive, which keeps the
+      // order), the scores stay unscaled: the row max is taken on them and
+      // scaled once, and each exponent below is one fma, s * c - m.
+      // Otherwise each score is masked and scaled first (c = 1 below).
       const uint64_t vm = ((uint64_t)masks[b * 2 + 1] << 32 | masks[b * 2]) >> (24 * wg);
+      float cl = scale_log2;
+      if ((uint32_t)(vm & 0xFFFFFFu) != 0xFFFFFFu || !(scale_log2 > 0.f)) {
+#pragma unroll
+        for (int j = 0; j < kBN / 2; ++j)
+          sp[j] = ((vm >> j) & 1u) ? sp[j] * scale_log2 : -INFINITY;
+        cl = 1.f;
+      }
       float hm = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < kBN / 2; ++j) {
-        sp[j] = ((vm >> j) & 1u) ? sp[j] * scale_log2 : -INFINITY;
-        hm = fmaxf(hm, sp[j]);
-      }
+      for (int j = 0; j < kBN / 2; ++j) hm = fmaxf(hm, sp[j]);
+      hm *= cl;
       float* rb = red + buf * 256;
       rb[wg * 128 + i] = hm;
       float alpha = 1.f;
@@ -524,7 +533,8 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
         for (int j = 0; j < kBN / 2; j += 2) {
           // The row sum uses the unrounded values (it sets the LSE); P goes
           // to the PV MMA in bf16.
-          const float e0 = ex2_approx(sp[j] - m_run), e1 = ex2_approx(sp[j + 1] - m_run);
+          const float e0 = ex2_approx(fmaf(sp[j], cl, -m_run));
+          const float e1 = ex2_approx(fmaf(sp[j + 1], cl, -m_run));
           pk[j / 2] = pack_bf16(e0, e1);
           lsum += e0 + e1;
         }
