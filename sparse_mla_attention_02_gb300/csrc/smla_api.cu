@@ -199,11 +199,11 @@ namespace smla {
 // Split plan.  Valid counts are device data, so ranges are cut over topk; a
 // range past a token's valid count yields an empty partial (0, -inf) that the
 // combine ignores.
-//  - tensor-core paths (keys-major for h <= 16, heads-major up to 128): one
-//    unit = (token, range) on a 2-SM cluster, one cluster per two SMs
-//    resident; split only when the tokens alone leave more than half of the
-//    pairs idle (each split costs partial-O traffic), or when topk is longer
-//    than one unit's range.
+//  - tensor-core paths: one unit = (token, range) on one CTA per SM
+//    (keys-major, h <= 16) or on a 2-SM cluster (heads-major, up to 128
+//    heads); split only when the tokens alone leave more than half of the
+//    SMs (or SM pairs) idle (each split costs partial-O traffic), or when
+//    topk is longer than one unit's range.
 //  - CUDA-core path: enough (token, 16-head group, range) units to fill every
 //    SM twice.
 Plan make_plan(int T, int h, int d_qk, int d_v, int topk, int kv_format,
@@ -213,11 +213,11 @@ Plan make_plan(int T, int h, int d_qk, int d_v, int topk, int kv_format,
   const bool keys = tc_keys_supported(h, d_qk, kv_format);
   if (keys || tc_supported(h, d_qk, kv_format)) {
     pl.kind = keys ? kKernelTcKeys : kKernelTc;
-    gran = keys ? 128 : 64;
+    gran = 64;
     const int max_range = keys ? tc_keys_max_range() : tc_max_range();
-    const int pairs = num_sms > 1 ? num_sms / 2 : 1;
-    if (2LL * T < pairs) {
-      splits = pairs / (T > 0 ? T : 1);
+    const int places = keys ? (num_sms > 0 ? num_sms : 1) : (num_sms > 1 ? num_sms / 2 : 1);
+    if (2LL * T < places) {
+      splits = places / (T > 0 ? T : 1);
       const int max_by_topk = (topk + 127) / 128;
       if (splits > max_by_topk) splits = max_by_topk;
       if (splits > 16) splits = 16;

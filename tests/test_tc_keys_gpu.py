@@ -1,14 +1,15 @@
 """Parity of the keys-major tensor-core kernel (h <= 16 heads) with the fp64
 oracle, through the C ABI.
 
-This kernel puts the 128 top-k positions of a block on the MMA's rows, keeps
-one fp32 score accumulator per 128-channel scale group, and exchanges partial
-scores between the two CTAs of a cluster; the cases below aim at what that
-design can get wrong: every cache format at both row widths, head counts that
-are not 16, ragged last blocks (1, 127, 128, 129 valid keys), top-k ranges
-longer than one unit (split + merge), many units per SM, scores that keep
-growing across blocks (the lazy running max must rescale O), and group scales
-over four decades.  Same bar as the other parity tests: max|dO| <= 2e-2,
+This kernel puts a block's 64 keys on the MMA's 128 rows (each key once per
+channel half), keeps one fp32 score accumulator per 128-channel scale group,
+and sums the two halves of a key's scores inside the CTA; the cases below aim
+at what that design can get wrong: every cache format at both row widths,
+head counts that are not 16 (or not 8, the heads a thread owns), ragged last
+blocks (1, 63, 64, 65, 127, 128, 129 valid keys), top-k ranges longer than
+one unit (split + merge), many units per SM, scores that keep growing across
+blocks (the lazy running max must rescale O), and group scales over four
+decades.  Same bar as the other parity tests: max|dO| <= 2e-2,
 max|dLSE| <= 1e-3, empty rows exactly (0, -inf).
 """
 import numpy as np
@@ -42,6 +43,15 @@ def test_formats_widths_heads(cuda_lib, kv_dtype, d_qk, h):
     check(cuda_lib, w)
 
 
+@pytest.mark.parametrize("kv_dtype", [0, 1, 2])
+@pytest.mark.parametrize("h", [9, 16])
+def test_block_edges(cuda_lib, kv_dtype, h):
+    """Valid counts at and around the 64-key block edge."""
+    w = W.custom(T=6, h=h, topk=200, num_slots=700, kv_dtype=kv_dtype,
+                 valid=[63, 64, 65, 191, 192, 2], seed=260 + kv_dtype + h)
+    check(cuda_lib, w)
+
+
 @pytest.mark.parametrize("kv_dtype", [0, 2])
 def test_topk_longer_than_one_unit_splits(cuda_lib, kv_dtype):
     """topk 3000 > 2048 positions per unit: at least two ranges per token,
@@ -57,8 +67,8 @@ def test_topk_longer_than_one_unit_splits(cuda_lib, kv_dtype):
 
 
 def test_many_units_per_sm_group_scales(cuda_lib):
-    """400 units of 1..256 keys on 76 clusters: every CTA runs several units
-    back to back (barrier phases, TMEM and the exchange buffers restart)."""
+    """400 units of 1..256 keys on the SMs: every SM runs several units back to
+    back (barrier phases, TMEM and the shared buffers restart)."""
     T = 400
     rng = np.random.default_rng(6)
     w = W.custom(T=T, h=16, topk=256, num_slots=3000, kv_dtype=2,
