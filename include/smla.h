@@ -259,6 +259,65 @@ SMLA_API smla_status smla_fwd_paged(const void* q, const void* kv_cache, int kv_
                            cudaStream_t stream);
 
 /*
+ * smla_fwd_host_workspace_size — bytes of device workspace smla_fwd_host
+ * needs for T tokens in chunks of chunk_tokens (0 = the default chunking):
+ * two slots of staging buffers for a chunk's q, indices, valid_len, O and
+ * LSE, plus the split workspace smla_fwd_ws needs for a chunk.  0 when
+ * T <= 0.
+ */
+SMLA_API size_t smla_fwd_host_workspace_size(int T, int h, int d_qk, int d_v,
+                                             int topk, int kv_dtype,
+                                             int chunk_tokens);
+
+/*
+ * smla_fwd_host — smla_fwd for a caller whose per-step tensors live in host
+ * memory: q, indices, valid_len are read from the host and O, LSE written to
+ * the host, with the copies overlapped with the forward.  The pages have no
+ * counterpart (their serving stacks keep these tensors on the device); it is
+ * the host-memory boundary of the same computation.
+ *
+ * The T tokens are processed in chunks of chunk_tokens (0: about T / 8, at
+ * least 256 and a multiple of 64).  While the forward of chunk i runs on
+ * `stream`, a library-owned stream copies chunk i + 1 in and another copies
+ * chunk i - 1 out; device staging is double-buffered in `workspace`.  Each
+ * chunk runs smla_fwd_ws on its tokens, so its rows are exactly what
+ * smla_fwd computes for that chunk; the split plan follows the chunk's
+ * size, so where a chunk splits its top-k ranges and one call on all T
+ * tokens would not (or the other way round), the rounding of those rows
+ * differs within the usual bounds.
+ *  q_host          bf16 [T, h, d_qk], host memory
+ *  kv_cache        device, as for smla_fwd (model state stays resident)
+ *  k_scale         device, as for smla_fwd
+ *  indices_host    int32 [T, topk], host memory
+ *  valid_len_host  int32 [T] host memory, or NULL as for smla_fwd
+ *  out_host        bf16 [T, h, d_v], host memory, written
+ *  lse_host        fp32 [T, h] host memory, or NULL
+ *  chunk_tokens    tokens per chunk, >= 0 (0 = default)
+ *  workspace       device, >= smla_fwd_host_workspace_size(...) bytes,
+ *                  256-byte aligned, caller-owned
+ * Host buffers should be page-locked (cudaHostAlloc / pinned): pageable
+ * memory is still correct but its copies do not overlap.
+ * Asynchronous on `stream`: the host buffers may be read or written until
+ * `stream` has been synchronised (the call ends with `stream` waiting for
+ * the last copies).  No allocation after the first call on a device, which
+ * creates the two copy streams and their events.  Calls are serialised
+ * inside the library (one copy pipeline per device); one workspace must not
+ * be shared by calls that may overlap on the GPU.
+ * Errors: those of smla_fwd for the shape and arguments (checked before
+ * anything is queued), SMLA_ERR_INVALID_ARG for NULL host buffers or a
+ * negative chunk_tokens, SMLA_ERR_WORKSPACE when the workspace is missing or
+ * too small, SMLA_ERR_CUDA.
+ */
+SMLA_API smla_status smla_fwd_host(const void* q_host, const void* kv_cache,
+                                   int kv_dtype, const float* k_scale,
+                                   const int32_t* indices_host,
+                                   const int32_t* valid_len_host, int T, int h,
+                                   int d_qk, int d_v, int topk, int64_t num_slots,
+                                   float sm_scale, void* out_host, float* lse_host,
+                                   int chunk_tokens, void* workspace,
+                                   size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * smla_combine — LSE-weighted merge of partial results computed over disjoint
  * key sets (the split-KV combine, and the cross-rank merge of the
  * flashmla_sparse page's DCP path):

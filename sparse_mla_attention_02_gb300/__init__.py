@@ -71,6 +71,10 @@ def load():
         lib.smla_fwd_split_q.argtypes = [P, P, P, I, P, F, P, P, I, I, I, I, I, I64, F,
                                          P, P, P, SZ, P]
         lib.smla_fwd_split_q.restype = I
+        lib.smla_fwd_host.argtypes = fwd_args + [I, P, SZ, P]
+        lib.smla_fwd_host.restype = I
+        lib.smla_fwd_host_workspace_size.argtypes = [I, I, I, I, I, I, I]
+        lib.smla_fwd_host_workspace_size.restype = SZ
         lib.smla_workspace_size.argtypes = [I, I, I, I, I, I]
         lib.smla_workspace_size.restype = SZ
         lib.smla_plan_info.argtypes = [I, I, I, I, I, I, ctypes.POINTER(I),
@@ -320,6 +324,60 @@ def smla_fwd_ws(q, kv_cache, kv_dtype, k_scale, indices, valid_len, sm_scale,
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.smla_fwd_ws(*args, _p(workspace), nbytes, _stream(stream)),
            "smla_fwd_ws")
+    return out, lse
+
+
+def smla_fwd_host_workspace_size(T, h, d_qk, topk, kv_dtype, d_v=512,
+                                 chunk_tokens=0) -> int:
+    return int(load().smla_fwd_host_workspace_size(T, h, d_qk, d_v, topk,
+                                                   kv_dtype, chunk_tokens))
+
+
+def smla_fwd_host(q, kv_cache, kv_dtype, k_scale, indices, valid_len, sm_scale,
+                  out=None, lse=None, want_lse=True, num_slots=None,
+                  chunk_tokens=0, workspace=None, stream=None):
+    """``smla_fwd_host``: q, indices, valid_len, out and lse are CPU tensors
+    (pin them for overlap); kv_cache and k_scale are device tensors.  The
+    copies and the forward are queued on ``stream`` (and the library's copy
+    streams); synchronise the stream before reading ``out``/``lse``.
+    ``workspace``: a device uint8 tensor of at least
+    smla_fwd_host_workspace_size(...) bytes, or None to allocate one."""
+    import torch
+    lib = load()
+    T, h, d_qk = q.shape
+    d_v = 512
+    if q.device.type != "cpu" or indices.device.type != "cpu" or \
+            (valid_len is not None and valid_len.device.type != "cpu"):
+        raise ValueError("smla_fwd_host: q, indices, valid_len live in host memory")
+    if q.dtype != torch.bfloat16 or not q.is_contiguous():
+        raise ValueError("q must be contiguous bf16 [T, h, d_qk]")
+    if indices.dtype != torch.int32 or not indices.is_contiguous() or \
+            indices.dim() != 2 or indices.shape[0] != T:
+        raise ValueError("indices must be contiguous int32 [T, topk]")
+    if valid_len is not None and (valid_len.dtype != torch.int32 or
+                                  valid_len.shape != (T,) or
+                                  not valid_len.is_contiguous()):
+        raise ValueError("valid_len must be contiguous int32 [T]")
+    topk = indices.shape[1]
+    S = _kv_slots(kv_cache, kv_dtype, k_scale, d_qk, num_slots)
+    if out is None:
+        out = torch.empty((T, h, d_v), dtype=torch.bfloat16, pin_memory=True)
+    if lse is None and want_lse:
+        lse = torch.empty((T, h), dtype=torch.float32, pin_memory=True)
+    for t in (out, lse):
+        if t is not None and (t.device.type != "cpu" or not t.is_contiguous()):
+            raise ValueError("out / lse must be contiguous host tensors")
+    nbytes = smla_fwd_host_workspace_size(T, h, d_qk, topk, kv_dtype, d_v,
+                                          chunk_tokens)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8,
+                                device=kv_cache.device)
+    _check(lib.smla_fwd_host(_p(q), _p(kv_cache), kv_dtype, _p(k_scale),
+                             _p(indices), _p(valid_len), T, h, d_qk, d_v, topk,
+                             S, float(sm_scale), _p(out), _p(lse),
+                             int(chunk_tokens), _p(workspace),
+                             workspace.numel(), _stream(stream)),
+           "smla_fwd_host")
     return out, lse
 
 
