@@ -276,7 +276,7 @@ SMLA_API size_t smla_fwd_host_workspace_size(int T, int h, int d_qk, int d_v,
  * counterpart (their serving stacks keep these tensors on the device); it is
  * the host-memory boundary of the same computation.
  *
- * The T tokens are processed in chunks of chunk_tokens (0: about T / 8, at
+ * The T tokens are processed in chunks of chunk_tokens (0: about T / 16, at
  * least 256 and a multiple of 64).  While the forward of chunk i runs on
  * `stream`, a library-owned stream copies chunk i + 1 in and another copies
  * chunk i - 1 out; device staging is double-buffered in `workspace`.  Each

@@ -53,11 +53,12 @@ smla_status host_pipe(HostPipe** out) {
   return SMLA_OK;
 }
 
-// Tokens per chunk: the caller's choice, else about an eighth of the batch
+// Tokens per chunk: the caller's choice, else about a sixteenth of the batch
 // (at least 256 tokens, a multiple of 64), so a long batch has enough chunks
-// to overlap and each chunk still fills the GPU.
+// to overlap and each chunk still fills the GPU.  (8192-token prefill on
+// GB300: 512-token chunks 8.3 ms a step, 256: 8.9, 1024: 8.9, 2048: 10.1.)
 int chunk_of(int T, int chunk_tokens) {
-  int c = chunk_tokens > 0 ? chunk_tokens : (T + 7) / 8;
+  int c = chunk_tokens > 0 ? chunk_tokens : (T + 15) / 16;
   if (chunk_tokens <= 0) {
     c = (c + 63) / 64 * 64;
     if (c < 256) c = 256;
