@@ -167,6 +167,7 @@ smla_status run_fwd(const void* q, const void* kv, int kv_dtype,
   p.split_len = plan.split_len;
   p.sm_scale = sm_scale;
   p.fp32_out = plan.splits > 1 || out_f32 ? 1 : 0;
+  p.lpt = plan.lpt;
   p.req_id = pg.req_id;
   p.block_table = pg.table;
   p.num_reqs = pg.num_reqs;
@@ -243,6 +244,13 @@ Plan make_plan(int T, int h, int d_qk, int d_v, int topk, int kv_format,
   splits = (topk + len - 1) / len;
   pl.splits = splits;
   pl.split_len = len;
+  // Longest-first unit order pays only when the units do not all run at
+  // once (and costs a pass over the valid counts at each CTA's start).
+  if (pl.kind != kKernelSimt) {
+    const int64_t n_units = (int64_t)T * splits;
+    const int64_t places = pl.kind == kKernelTcKeys ? num_sms : num_sms / 2;
+    pl.lpt = (n_units > places && n_units <= 4096) ? 1 : 0;
+  }
   pl.workspace_bytes =
       splits > 1 ? sizeof(float) * (size_t)splits * T * h * (d_v + 1) : 0;
   return pl;

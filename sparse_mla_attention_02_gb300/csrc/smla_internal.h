@@ -39,6 +39,8 @@ struct FwdParams {
   int T, h, d_qk, d_v, topk;
   int splits;             // top-k position ranges per (token, head group)
   int split_len;          // positions per range
+  int lpt;                // take the units longest first (lpt_unit): more
+                          // units than run at once, at most kLptMaxUnits
   int fp32_out;           // write normalised fp32 O and LSE to o_part / lse_part
                           // (split s at s * T * h rows): splits > 1, or
                           // smla_fwd_partial (splits == 1, caller's buffers)
@@ -107,6 +109,7 @@ struct Plan {
   int splits;
   int split_len;
   size_t workspace_bytes;   // partial O and LSE for splits > 1, else 0
+  int lpt;                  // longest-first unit order (see FwdParams::lpt)
 };
 
 Plan make_plan(int T, int h, int d_qk, int d_v, int topk, int kv_format,

@@ -125,6 +125,9 @@ struct TcArgs {
   float scale_log2; // sm_scale * log2(e)
 };
 
+// kLpt: the units are taken longest first (lpt_unit); a separate instance,
+// so that launches in unit order carry none of its code.
+template <bool kLpt>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 smla_tc_kernel(const __grid_constant__ TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -137,7 +140,10 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
   const uint32_t peer = r ^ 1u;
 
   // ---- a1: work unit ------------------------------------------------------
-  const int unit = blockIdx.x >> 1;
+  // (kLpt: the units are taken longest first; the slot-id area is the
+  // scratch, before it is filled)
+  int unit = (int)(blockIdx.x >> 1);
+  if (kLpt) unit = lpt_unit(p, unit, p.T * p.splits, kBN, reinterpret_cast<int*>(sm + kOffSlot));
   const int split = unit % p.splits;
   const int t = unit / p.splits;
   int v = p.topk;
@@ -703,11 +709,12 @@ cudaError_t launch_tc(const FwdParams& p, cudaStream_t stream) {
   a.scale_log2 = p.sm_scale * 1.4426950408889634f;
   const int64_t clusters = (int64_t)p.T * p.splits;
   if (clusters * 2 > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  cudaError_t e = cudaFuncSetAttribute(smla_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const bool lpt = p.lpt && clusters <= kLptMaxUnits;
+  auto kernel = lpt ? smla_tc_kernel<true> : smla_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  smla_tc_kernel<<<(unsigned)(clusters * 2), kThreads, kSmemBytes, stream>>>(a);
+  kernel<<<(unsigned)(clusters * 2), kThreads, kSmemBytes, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -155,7 +155,9 @@ __device__ __forceinline__ float xreduce8(float (&v)[8], int lane) {
   return op2<kMax>(x, __shfl_xor_sync(0xffffffffu, x, 16));
 }
 
-template <int kFmt>
+// kLpt: the units are taken longest first (lpt_unit); a separate instance,
+// so that launches in unit order carry none of its code.
+template <int kFmt, bool kLpt>
 __global__ void __launch_bounds__(kThreads, 1)
 smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
   // Formats with per-(slot, group) scales: one QK accumulator per group.
@@ -173,7 +175,10 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // ---- a1: work unit ------------------------------------------------------
-  const int unit = blockIdx.x;
+  // (kLpt: the units are taken longest first; the slot-id area is the
+  // scratch, before it is filled)
+  int unit = (int)blockIdx.x;
+  if (kLpt) unit = lpt_unit(p, unit, p.T * p.splits, kBK, reinterpret_cast<int*>(sm + kOffSlot));
   const int split = unit % p.splits;
   const int t = unit / p.splits;
   int v = p.topk;
@@ -775,11 +780,12 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
 
 template <int kFmt>
 cudaError_t launch_keys(const KeysArgs& a, unsigned blocks, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(smla_tc_keys_kernel<kFmt>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const bool lpt = a.p.lpt && blocks <= (unsigned)kLptMaxUnits;
+  auto kernel = lpt ? smla_tc_keys_kernel<kFmt, true> : smla_tc_keys_kernel<kFmt, false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  smla_tc_keys_kernel<kFmt><<<blocks, kThreads, kSmemBytes, stream>>>(a);
+  kernel<<<blocks, kThreads, kSmemBytes, stream>>>(a);
   return cudaGetLastError();
 }
 

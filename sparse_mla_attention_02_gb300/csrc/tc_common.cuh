@@ -202,6 +202,86 @@ __device__ __forceinline__ bool load_unit_slots(const FwdParams& p, int t, int k
                        pt, nthr);
 }
 
+// Longest-first unit order for launches of at most kLptMaxUnits units.  A
+// unit u = (token u / splits, range u % splits) has ceil(n / bn) blocks of
+// work, n = the valid positions of its range.  The block scheduler starts
+// CTAs (clusters) roughly in index order, so when the unit sizes vary, a
+// late large unit sets the end of the launch; taking the units in
+// decreasing size instead lets the small ones fill in at the end.  Every
+// thread of the CTA calls this with the same `rank` (the CTA's or cluster's
+// index) and gets the unit at that rank of the order: units sorted by
+// decreasing block count, ties in unit order.  The result depends only on
+// (rank, valid_len, the plan), so the CTAs of a cluster agree and every unit
+// is taken exactly once.  `scratch` is shared memory for (kLptMaxBlocks + 2)
+// + nthr / 32 + 1 ints; the call ends with a block-wide barrier.
+constexpr int kLptMaxUnits = 4096;
+constexpr int kLptMaxBlocks = 64;
+__device__ __forceinline__ int unit_blocks(const FwdParams& p, int u, int bn) {
+  const int t = u / p.splits, sp = u - t * p.splits;
+  int v = p.topk;
+  if (p.valid_len) v = min(max(__ldg(p.valid_len + t), 0), p.topk);
+  const int k0 = sp * p.split_len, k1 = min(k0 + p.split_len, v);
+  return k1 > k0 ? min((k1 - k0 + bn - 1) / bn, kLptMaxBlocks) : 0;
+}
+static __device__ __noinline__ int lpt_unit(const FwdParams& p, int rank, int n_units, int bn,
+                                        int* scratch) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5, nwarp = (nthr + 31) >> 5;
+  int* hist = scratch;                             // [kLptMaxBlocks + 1]
+  int* sel = scratch + kLptMaxBlocks + 1;          // [0] bucket, [1] index in it, then the unit
+  int* wsum = sel + 2;                             // [nwarps]
+  for (int c = tid; c <= kLptMaxBlocks; c += nthr) hist[c] = 0;
+  __syncthreads();
+  for (int u = tid; u < n_units; u += nthr) atomicAdd(&hist[unit_blocks(p, u, bn)], 1);
+  __syncthreads();
+  if (tid == 0) {                                  // the bucket holding `rank`
+    int start = 0, c = kLptMaxBlocks;
+    for (; c > 0 && start + hist[c] <= rank; --c) start += hist[c];
+    sel[0] = c;
+    sel[1] = rank - start;
+  }
+  __syncthreads();
+  const int cb = sel[0], k = sel[1];
+  // Every unit the same size: the order is the unit order.
+  if (hist[cb] == n_units) {
+    __syncthreads();
+    return rank;
+  }
+  // The k-th unit (in unit order) of bucket cb: each thread counts its chunk
+  // of units, a block-wide scan places the chunks, and the thread whose
+  // chunk holds it writes it.
+  const int per = (n_units + nthr - 1) / nthr;
+  const int u0 = tid * per, u1 = min(u0 + per, n_units);
+  int cnt = 0;
+  for (int u = u0; u < u1; ++u) cnt += unit_blocks(p, u, bn) == cb;
+  int inc = cnt;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, inc, d);
+    if (lane >= d) inc += y;
+  }
+  if (lane == 31) wsum[warp] = inc;
+  __syncthreads();
+  int before = inc - cnt;
+  for (int w = 0; w < warp; ++w) before += wsum[w];
+  if (k >= before && k < before + cnt) {
+    int seen = before;
+    for (int u = u0; u < u1; ++u) {
+      if (unit_blocks(p, u, bn) == cb) {
+        if (seen == k) {
+          sel[0] = u;
+          break;
+        }
+        ++seen;
+      }
+    }
+  }
+  __syncthreads();
+  const int unit = sel[0];
+  __syncthreads();
+  return unit;
+}
+
 // A bf16 cache [num_slots, d_qk] as a 2-D tensor with 64-channel x 1-row
 // boxes and the 128-byte swizzle of the MMA operand tiles (TMA tile::gather4
 // reads four such rows per instruction; a row id of -1 reads zeros).
