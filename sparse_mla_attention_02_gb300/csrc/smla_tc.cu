@@ -102,6 +102,7 @@ enum {
   kBarODone = kBarXCons + 2,
   kBarOFinal,                          // one phase: the unit's last PV is done
   kBarQReady,
+  kBarQStaged,                         // the staged Q rows have been read
   kNumBars
 };
 constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
@@ -111,6 +112,11 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kColS + 2 * kBN <= kTmemCols, "TMEM budget");
 static_assert(kAtomBytes % 1024 == 0, "swizzle atoms must stay 1024-aligned");
 static_assert(kBN % 12 == 0, "three producer warps split the 4-row groups evenly");
+// Q staging: the CTA's Q half as 128 rows of up to 288 channels (row stride
+// 592 bytes), in gather stages 1..3, which are idle until Q is in TMEM.
+constexpr uint32_t kQStageRow = 592;
+constexpr uint32_t kOffQStage = kOffTile + kTileBytes;
+static_assert(kOffQStage + 128 * kQStageRow <= kOffTile + kStages * kTileBytes, "Q staging");
 
 struct TcArgs {
   CUtensorMap kv_map;  // bf16 cache as a 2-D tensor [num_slots, d_qk], 64-channel boxes
@@ -157,6 +163,34 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffAbort);
   Waiter W{abort_flag, p.status};
 
+  // Q half, first step (bf16 caches): the 256 softmax threads copy the
+  // CTA's Q half (128 heads x 2 * ksteps 16-byte pieces) into the staging
+  // rows, consecutive threads on consecutive pieces of a head row
+  // (coalesced), before the set-up below; heads >= h are zero.  The rows go
+  // to TMEM after it.  (E4M3 caches load Q per head after the set-up: their
+  // converters fill stages 1..3 early, and staging measured slower there.)
+  if (!a.fp8 && warp >= 4 && warp <= 11) {
+    const int st = tid - 128;
+    const int per_row = 2 * a.ksteps;                     // 36 or 32 pieces
+#pragma unroll
+    for (int k0 = 0; k0 < 18; k0 += 9) {                 // two batches of 9 loads
+      uint4 qv[9];
+#pragma unroll
+      for (int k = 0; k < 9; ++k) {
+        const int e = st + 256 * (k0 + k), hd = e / per_row, c16 = e - hd * per_row;
+        qv[k] = (hd < p.h && e < 128 * per_row)
+                    ? __ldg(q_chunk(p, t, hd, a.q_lo[r] + 8 * c16))
+                    : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int k = 0; k < 9; ++k) {
+        const int e = st + 256 * (k0 + k), hd = e / per_row, c16 = e - hd * per_row;
+        if (e < 128 * per_row)
+          *reinterpret_cast<uint4*>(sm + kOffQStage + hd * kQStageRow + 16 * c16) = qv[k];
+      }
+    }
+  }
+
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       // bf16: one expect_tx per TMA warp; fp8: one arrival per converter thread
@@ -176,6 +210,7 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
     mbar_init(bar(kBarODone), 1);
     mbar_init(bar(kBarOFinal), 1);
     mbar_init(bar(kBarQReady), 256);
+    mbar_init(bar(kBarQStaged), 256);
     *abort_flag = 0;
     fence_mbar_init_cluster();
   }
@@ -344,6 +379,7 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
     for (int b = 0; b < nb; ++b) {
       const int s = b % kStages;
       if (b >= kStages) W.wait(bar(kBarKvEmpty + s), ((b / kStages) - 1) & 1);
+      if (b >= 1 && b < kStages) W.wait(bar(kBarQStaged), 0);   // Q staging read
       __syncwarp();
       if (elect_one()) {
         const uint32_t full = bar(kBarKvFull + s);
@@ -387,27 +423,33 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
     // Q half -> TMEM (rows >= h are zero): 16-column groups [0, 5) by the
     // first warpgroup, [5, ksteps / 2) by the second.
     {
-      const int hq = head < p.h ? head : 0;
+      // (staged before the set-up; the block-wide barrier since then makes
+      // every thread's staging stores visible)
       const int g0 = wg == 0 ? 0 : 5, g1 = wg == 0 ? 5 : a.ksteps / 2;
-      uint4 qv[20];
-#pragma unroll
-      for (int c = 0; c < 20; ++c)
-        qv[c] = (head < p.h && c < 4 * (g1 - g0))
-                    ? __ldg(q_chunk(p, t, hq, a.q_lo[r] + 8 * (4 * g0 + c)))
-                    : make_uint4(0u, 0u, 0u, 0u);
-      __syncwarp();
+      const uint8_t* qrow = sm + kOffQStage + head * kQStageRow;
 #pragma unroll
       for (int k = 0; k < 5; ++k) {
         if (k < g1 - g0) {                       // same for every lane
-          const uint32_t w[16] = {qv[4 * k].x,     qv[4 * k].y,     qv[4 * k].z,
-                                  qv[4 * k].w,     qv[4 * k + 1].x, qv[4 * k + 1].y,
-                                  qv[4 * k + 1].z, qv[4 * k + 1].w, qv[4 * k + 2].x,
-                                  qv[4 * k + 2].y, qv[4 * k + 2].z, qv[4 * k + 2].w,
-                                  qv[4 * k + 3].x, qv[4 * k + 3].y, qv[4 * k + 3].z,
-                                  qv[4 * k + 3].w};
+          uint4 x0, x1, x2, x3;
+          if (a.fp8) {                           // from global memory, this head's row
+            const int c0 = a.q_lo[r] + 32 * (g0 + k);
+            const bool live = head < p.h;
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            x0 = live ? __ldg(q_chunk(p, t, head, c0)) : z;
+            x1 = live ? __ldg(q_chunk(p, t, head, c0 + 8)) : z;
+            x2 = live ? __ldg(q_chunk(p, t, head, c0 + 16)) : z;
+            x3 = live ? __ldg(q_chunk(p, t, head, c0 + 24)) : z;
+          } else {                               // from the staging rows
+            const uint4* q4 = reinterpret_cast<const uint4*>(qrow + 64 * (g0 + k));
+            x0 = q4[0]; x1 = q4[1]; x2 = q4[2]; x3 = q4[3];
+          }
+          const uint32_t w[16] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
+                                  x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
+          __syncwarp();
           tmem_st16(tmem + lane_base + kColQ + 16 * (g0 + k), w);
         }
       }
+      mbar_arrive(bar(kBarQStaged));             // the staging may be overwritten
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(kBarQReady));
