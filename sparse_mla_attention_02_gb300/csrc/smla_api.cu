@@ -245,10 +245,14 @@ Plan make_plan(int T, int h, int d_qk, int d_v, int topk, int kv_format,
   pl.splits = splits;
   pl.split_len = len;
   // Longest-first unit order pays only when the units do not all run at
-  // once (and costs a pass over the valid counts at each CTA's start).
-  if (pl.kind != kKernelSimt) {
+  // once (and costs a pass over the valid counts at each CTA's start).  The
+  // keys-major kernel keeps the unit order: its units are short next to a
+  // launch on 152 SMs, and neighbouring tokens that select overlapping
+  // slots then run together and share L2 (a 2048-token mixed batch read
+  // 2.3x the DRAM bytes longest first).
+  if (pl.kind == kKernelTc) {
     const int64_t n_units = (int64_t)T * splits;
-    const int64_t places = pl.kind == kKernelTcKeys ? num_sms : num_sms / 2;
+    const int64_t places = num_sms / 2;
     pl.lpt = (n_units > places && n_units <= 4096) ? 1 : 0;
   }
   pl.workspace_bytes =
