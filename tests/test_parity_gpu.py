@@ -282,3 +282,32 @@ def test_full_config_sampled(cuda_lib, name, n_rand):
     assert torch.equal(torch.isfinite(L).all(dim=1), v > 0)
     del w, O, L
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("kv_dtype,h,topk", [(0, 128, 2048), (1, 64, 2048), (0, 32, 4000)])
+def test_longest_first_order_variable_units(cuda_lib, kv_dtype, h, topk):
+    """More units than clusters, with valid counts that vary (0 .. topk):
+    the heads-major kernel takes the units longest first, each CTA finding
+    its own unit from a histogram of the valid counts.  Every row must be
+    written (outputs start as NaN) with its own token's result (checked
+    against the oracle on a sample of tokens); topk 4000 also splits each
+    row into two ranges, so the units are (token, range) pairs of different
+    lengths merged by the combine."""
+    T = 160
+    rng = np.random.default_rng(70 + h)
+    valid = rng.integers(0, topk + 1, size=T)
+    valid[:3] = [topk, 0, 1]
+    w = W.custom(T=T, h=h, topk=topk, num_slots=4096, kv_dtype=kv_dtype,
+                 valid=valid, seed=71 + h, name=f"lpt_h{h}")
+    assert cuda_lib.smla_plan_info(T, h, 576, topk, kv_dtype)["kernel"] == "tc_heads"
+    wd = w.to("cuda")
+    out = torch.full((T, h, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((T, h), float("nan"), dtype=torch.float32, device="cuda")
+    cuda_lib.smla_fwd(wd.q, wd.kv, wd.kv_dtype, wd.k_scale, wd.indices,
+                      wd.valid_len, wd.sm_scale, out=out, lse=lse,
+                      num_slots=wd.num_slots)
+    torch.cuda.synchronize()
+    assert not torch.isnan(out).any() and not torch.isnan(lse).any()
+    sel = sorted(set(range(0, T, 7)) | {0, 1, 2, T - 1})
+    Or, Lr = oracle_fwd(w, tokens=sel)
+    compare(out[sel], lse[sel], Or, Lr, w.name)
