@@ -103,6 +103,7 @@ enum {
   kBarOFinal,                          // one phase: the unit's last PV is done
   kBarQReady,
   kBarQStaged,                         // the staged Q rows have been read
+  kBarQLoaded,                         // the Q boxes have landed (TMA staging)
   kNumBars
 };
 constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
@@ -120,6 +121,8 @@ static_assert(kOffQStage + 128 * kQStageRow <= kOffTile + kStages * kTileBytes, 
 
 struct TcArgs {
   CUtensorMap kv_map;  // bf16 cache as a 2-D tensor [num_slots, d_qk], 64-channel boxes
+  CUtensorMap q_map;   // q as a 2-D tensor [T * 128, d_qk], 64-channel x 128-row boxes
+  int q_tma;           // 1: Q staged by TMA boxes (bf16 cache, h = 128, q concatenated)
   FwdParams p;
   int fp8;          // 1: E4M3 cache with a per-tensor scale (converted on load)
   int g_lo[2];      // first cache channel gathered by CTA r
@@ -169,7 +172,7 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
   // (coalesced), before the set-up below; heads >= h are zero.  The rows go
   // to TMEM after it.  (E4M3 caches load Q per head after the set-up: their
   // converters fill stages 1..3 early, and staging measured slower there.)
-  if (!a.fp8 && warp >= 4 && warp <= 11) {
+  if (!a.fp8 && !a.q_tma && warp >= 4 && warp <= 11) {
     const int st = tid - 128;
     const int per_row = 2 * a.ksteps;                     // 36 or 32 pieces
 #pragma unroll
@@ -211,8 +214,18 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
     mbar_init(bar(kBarOFinal), 1);
     mbar_init(bar(kBarQReady), 256);
     mbar_init(bar(kBarQStaged), 256);
+    mbar_init(bar(kBarQLoaded), 1);
     *abort_flag = 0;
     fence_mbar_init_cluster();
+    if (a.q_tma) {
+      // The CTA's Q half as 128-row boxes of 64 channels (128-byte swizzle)
+      // into the staging area; channels past d_qk read as zeros.
+      const int nbox = (a.ksteps * 16 + 63) / 64;
+      mbar_arrive_expect_tx(bar(kBarQLoaded), (uint32_t)(nbox * 128 * 128));
+      for (int k = 0; k < nbox; ++k)
+        tma_load_2d(sb + kOffQStage + (uint32_t)k * 128u * 128u, &a.q_map, a.q_lo[r] + 64 * k,
+                    t * 128, bar(kBarQLoaded));
+    }
   }
   __syncwarp();
   if (warp == 0) {
@@ -427,6 +440,7 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
       // every thread's staging stores visible)
       const int g0 = wg == 0 ? 0 : 5, g1 = wg == 0 ? 5 : a.ksteps / 2;
       const uint8_t* qrow = sm + kOffQStage + head * kQStageRow;
+      if (a.q_tma) W.wait(bar(kBarQLoaded), 0);
 #pragma unroll
       for (int k = 0; k < 5; ++k) {
         if (k < g1 - g0) {                       // same for every lane
@@ -439,6 +453,16 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
             x1 = live ? __ldg(q_chunk(p, t, head, c0 + 8)) : z;
             x2 = live ? __ldg(q_chunk(p, t, head, c0 + 16)) : z;
             x3 = live ? __ldg(q_chunk(p, t, head, c0 + 24)) : z;
+          } else if (a.q_tma) {                  // from the swizzled TMA boxes
+            // channels [32 (g0 + k), +32): box (g0 + k) / 2, 16-byte chunks
+            // 4 ((g0 + k) % 2) + j, stored at chunk ^ (head % 8)
+            const int g = g0 + k;
+            const uint8_t* brow = sm + kOffQStage + (g >> 1) * 128 * 128 + head * 128;
+            const uint32_t sw = (uint32_t)head & 7u, c0 = 4u * (uint32_t)(g & 1);
+            x0 = *reinterpret_cast<const uint4*>(brow + (((c0 + 0u) ^ sw) << 4));
+            x1 = *reinterpret_cast<const uint4*>(brow + (((c0 + 1u) ^ sw) << 4));
+            x2 = *reinterpret_cast<const uint4*>(brow + (((c0 + 2u) ^ sw) << 4));
+            x3 = *reinterpret_cast<const uint4*>(brow + (((c0 + 3u) ^ sw) << 4));
           } else {                               // from the staging rows
             const uint4* q4 = reinterpret_cast<const uint4*>(qrow + 64 * (g0 + k));
             x0 = q4[0]; x1 = q4[1]; x2 = q4[2]; x3 = q4[3];
@@ -736,6 +760,22 @@ cudaError_t launch_tc(const FwdParams& p, cudaStream_t stream) {
   if (!a.fp8) {
     const cudaError_t e = encode_bf16_rows_map(&a.kv_map, p.kv, p.d_qk, p.num_slots);
     if (e != cudaSuccess) return e;
+  }
+  // Q by TMA boxes: bf16 cache, 128 heads (a token's rows are exactly one
+  // box high), q in one tensor.
+  if (!a.fp8 && p.h == 128 && !p.q_pe) {
+    auto encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)p.d_qk, (cuuint64_t)p.T * 128};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.d_qk * 2};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&a.q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.q), dims,
+               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    a.q_tma = 1;
   }
   if (p.d_qk == 576) {
     a.g_lo[0] = 0;   a.n_boxes[0] = 5; a.qk_lo[0] = 0;  a.q_lo[0] = 0;

@@ -165,6 +165,16 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int 
       : "memory");
 }
 
+// TMA tiled 2-D load of one box at coordinates (x, y), counted on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
 // Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to
 // another CTA's, counted on that CTA's mbarrier (complete_tx).
 __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src_cta,
