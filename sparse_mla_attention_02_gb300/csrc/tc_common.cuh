@@ -226,7 +226,7 @@ __device__ __forceinline__ int unit_blocks(const FwdParams& p, int u, int bn) {
 static __device__ __noinline__ int lpt_unit(const FwdParams& p, int rank, int n_units, int bn,
                                         int* scratch) {
   const int tid = threadIdx.x, nthr = blockDim.x;
-  const int lane = tid & 31, warp = tid >> 5, nwarp = (nthr + 31) >> 5;
+  const int lane = tid & 31, warp = tid >> 5;
   int* hist = scratch;                             // [kLptMaxBlocks + 1]
   int* sel = scratch + kLptMaxBlocks + 1;          // [0] bucket, [1] index in it, then the unit
   int* wsum = sel + 2;                             // [nwarps]
