@@ -38,8 +38,17 @@
 // elected lane per batch of MMAs) and owns TMEM; warps 1..3 load the unit's
 // slot ids, then gather with TMA; warps 4..7 and 8..11 are two softmax
 // warpgroups (thread i <-> TMEM lane i <-> head i; positions 0..23 and 24..47
-// of each block), which run the exchange, softmax, O rescale and the
-// epilogue; warp 12 signals the peer when its partial scores were consumed.
+// of each block), which move Q to TMEM and run the exchange, softmax, O
+// rescale and the epilogue; warp 12 signals the peer when its partial scores
+// were consumed.
+// Q reaches TMEM from shared memory for bf16 caches: with 128 heads and q in
+// one tensor, the CTA's Q half arrives as TMA boxes issued by the thread
+// that sets up the barriers; otherwise the softmax threads copy it with
+// coalesced loads before the set-up.  Either way it is staged in gather
+// stages 1..3, which the producers fill only after the rows were read.  With
+// E4M3 caches each softmax thread loads its head's row from global memory.
+// Launches with more units than clusters (and at most 4096 units) take the
+// units longest first (lpt_unit, the kLpt instance).
 // Every wait is bounded; a wait that runs out records a timeout status, sets
 // an abort flag that skips later waits, and the block finishes normally.
 #include <cuda.h>
