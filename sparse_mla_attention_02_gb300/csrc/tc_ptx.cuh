@@ -1,6 +1,7 @@
-// tc_ptx.cuh — inline-PTX wrappers for sm_103a: mbarriers, cp.async with
-// zero fill, cluster shared-memory access, and the 5th-generation tensor core
-// (tcgen05: TMEM allocation, MMA, commit, TMEM loads/stores).
+// tc_ptx.cuh — inline-PTX wrappers for sm_103a: mbarriers (bounded waits),
+// cluster shared-memory addressing, TMA (tile::gather4 and tiled 2-D loads,
+// bulk copies to the peer CTA), and the 5th-generation tensor core (tcgen05:
+// TMEM allocation, MMA, commit, TMEM loads/stores).
 //
 // Encodings follow the public PTX ISA (tcgen05 shared-memory matrix
 // descriptor and instruction descriptor for .kind::f16).
@@ -55,20 +56,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking probe: true when the phase with this parity has completed.
-// (try_wait may suspend the thread for a while; test_wait never does.)
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Cluster-scope acquire variant (for arrivals made by the peer CTA).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -110,23 +97,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
-// -------------------------------------------------------------- cp.async --
-
-// 16-byte global -> shared copy; src_bytes = 0 writes 16 zero bytes.
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src,
-                                            uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-
-// The mbarrier receives one arrival once all prior cp.async of this thread
-// have landed (the arrival is not counted in advance: .noinc).
-__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-
 // ------------------------------------------------------------- cluster --
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -140,17 +110,6 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
-}
-
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b,
-                                              uint32_t c, uint32_t d) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a),
-               "r"(b), "r"(c), "r"(d)
-               : "memory");
-}
-
-__device__ __forceinline__ void st_cluster_b32(uint32_t addr, uint32_t a) {
-  asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(addr), "r"(a) : "memory");
 }
 
 // TMA gather: four rows (y0..y3) of a 2-D tensor map, one box of columns
@@ -191,19 +150,6 @@ __device__ __forceinline__ void bulk_commit_group() {
 // Wait until every committed bulk copy of this thread has read its source.
 __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-// Asynchronous 16-byte store into another CTA's shared memory; its bytes are
-// counted on that CTA's mbarrier (complete_tx), which the receiver arms with
-// the expected byte count.
-__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, uint32_t b,
-                                            uint32_t c, uint32_t d,
-                                            uint32_t cluster_bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, "
-      "%4}, [%5];" ::"r"(cluster_addr),
-      "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
-      : "memory");
 }
 
 // Hint: bring the cache line holding src into L2 without waiting for it.
