@@ -306,7 +306,9 @@ SMLA_API size_t smla_fwd_host_workspace_size(int T, int h, int d_qk, int d_v,
  * Errors: those of smla_fwd for the shape and arguments (checked before
  * anything is queued), SMLA_ERR_INVALID_ARG for NULL host buffers or a
  * negative chunk_tokens, SMLA_ERR_WORKSPACE when the workspace is missing or
- * too small, SMLA_ERR_CUDA.
+ * too small, SMLA_ERR_CUDA.  An error after copies were queued returns only
+ * once those copies have finished (a host synchronisation of the copy
+ * streams), so the host buffers are free to release.
  */
 SMLA_API smla_status smla_fwd_host(const void* q_host, const void* kv_cache,
                                    int kv_dtype, const float* k_scale,

@@ -132,6 +132,13 @@ smla_status smla_fwd_host(const void* q_host, const void* kv_cache, int kv_dtype
   const size_t q_row = (size_t)h * d_qk * 2, o_row = (size_t)h * d_v * 2;
 
   auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  // On an error after copies were queued, wait for them before returning,
+  // so that no queued copy touches the caller's host buffers afterwards.
+  auto fail = [&](smla_status code) {
+    cudaStreamSynchronize(hp->s_in);
+    cudaStreamSynchronize(hp->s_out);
+    return code;
+  };
   // Nothing of this call starts before the caller's earlier work on `stream`.
   if (!ok(cudaEventRecord(hp->ev_start, stream)) ||
       !ok(cudaStreamWaitEvent(hp->s_in, hp->ev_start, 0)) ||
@@ -147,7 +154,8 @@ smla_status smla_fwd_host(const void* q_host, const void* kv_cache, int kv_dtype
     uint8_t* out_d = slot[s] + L.q + L.idx + L.vl;
     float* lse_d = reinterpret_cast<float*>(slot[s] + L.q + L.idx + L.vl + L.out);
     // copy in (after the forward that last read this slot)
-    if (i >= 2 && !ok(cudaStreamWaitEvent(hp->s_in, hp->ev_comp[s], 0))) return SMLA_ERR_CUDA;
+    if (i >= 2 && !ok(cudaStreamWaitEvent(hp->s_in, hp->ev_comp[s], 0)))
+      return fail(SMLA_ERR_CUDA);
     if (!ok(cudaMemcpyAsync(q_d, qh + (size_t)t0 * q_row, (size_t)n * q_row,
                             cudaMemcpyHostToDevice, hp->s_in)) ||
         !ok(cudaMemcpyAsync(idx_d, indices_host + (size_t)t0 * topk, (size_t)n * topk * 4,
@@ -155,16 +163,16 @@ smla_status smla_fwd_host(const void* q_host, const void* kv_cache, int kv_dtype
         (valid_len_host && !ok(cudaMemcpyAsync(vl_d, valid_len_host + t0, (size_t)n * 4,
                                                cudaMemcpyHostToDevice, hp->s_in))) ||
         !ok(cudaEventRecord(hp->ev_in[s], hp->s_in)))
-      return SMLA_ERR_CUDA;
+      return fail(SMLA_ERR_CUDA);
     // forward (after its inputs, and after the copy-out that last read this slot)
     if (!ok(cudaStreamWaitEvent(stream, hp->ev_in[s], 0)) ||
         (i >= 2 && !ok(cudaStreamWaitEvent(stream, hp->ev_out[s], 0))))
-      return SMLA_ERR_CUDA;
+      return fail(SMLA_ERR_CUDA);
     st = smla_fwd_ws(q_d, kv_cache, kv_dtype, k_scale, idx_d, valid_len_host ? vl_d : nullptr,
                      n, h, d_qk, d_v, topk, num_slots, sm_scale, out_d,
                      lse_host ? lse_d : nullptr, split_ws, L.split, stream);
-    if (st != SMLA_OK) return st;
-    if (!ok(cudaEventRecord(hp->ev_comp[s], stream))) return SMLA_ERR_CUDA;
+    if (st != SMLA_OK) return fail(st);
+    if (!ok(cudaEventRecord(hp->ev_comp[s], stream))) return fail(SMLA_ERR_CUDA);
     // copy out
     if (!ok(cudaStreamWaitEvent(hp->s_out, hp->ev_comp[s], 0)) ||
         !ok(cudaMemcpyAsync(oh + (size_t)t0 * o_row, out_d, (size_t)n * o_row,
@@ -172,12 +180,12 @@ smla_status smla_fwd_host(const void* q_host, const void* kv_cache, int kv_dtype
         (lse_host && !ok(cudaMemcpyAsync(lse_host + (size_t)t0 * h, lse_d, (size_t)n * h * 4,
                                          cudaMemcpyDeviceToHost, hp->s_out))) ||
         !ok(cudaEventRecord(hp->ev_out[s], hp->s_out)))
-      return SMLA_ERR_CUDA;
+      return fail(SMLA_ERR_CUDA);
   }
   // The caller's stream waits for the last copies out of both slots.
   if (!ok(cudaStreamWaitEvent(stream, hp->ev_out[(n_chunks - 1) & 1], 0)) ||
       (n_chunks > 1 && !ok(cudaStreamWaitEvent(stream, hp->ev_out[n_chunks & 1], 0))))
-    return SMLA_ERR_CUDA;
+    return fail(SMLA_ERR_CUDA);
   return SMLA_OK;
 }
 
