@@ -185,3 +185,65 @@ def test_split_q_argument_checks(lib):
     assert f(kv_dtype=3, d_qk=512) == 2
     assert f(kv_dtype=5) == 2
     assert f(T=0, qn=None, qp=None) == 0
+
+
+def _fwd_host(lib, **kw):
+    a = dict(q=1 << 12, kv=1 << 12, kv_dtype=0, k_scale=None, idx=1 << 12,
+             valid=None, T=4, h=16, d_qk=576, d_v=512, topk=64, S=256,
+             scale=0.04, out=1 << 12, lse=None, chunk=0, ws=1 << 12,
+             ws_bytes=1 << 30)
+    a.update(kw)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.smla_fwd_host(
+        P(a["q"]), P(a["kv"]), a["kv_dtype"], P(a["k_scale"]), P(a["idx"]),
+        P(a["valid"]), a["T"], a["h"], a["d_qk"], a["d_v"], a["topk"], a["S"],
+        a["scale"], P(a["out"]), P(a["lse"]), a["chunk"], P(a["ws"]),
+        a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=-1), 1), (dict(h=0), 1), (dict(topk=0), 1), (dict(S=0), 1),
+    (dict(chunk=-1), 1), (dict(h=129), 2), (dict(d_qk=128), 2),
+    (dict(d_v=256), 2), (dict(kv_dtype=5), 2), (dict(kv_dtype=3, d_qk=512), 2),
+])
+def test_host_entry_shape_errors_come_before_any_device_call(lib, kw, code):
+    assert _fwd_host(lib, **kw) == code
+
+
+def test_host_workspace_size_covers_two_staging_slots(lib):
+    """Whatever the split plan adds, the workspace holds two chunks' worth of
+    q, indices, valid counts, O and LSE (the copy of one chunk overlaps the
+    forward of the other)."""
+    f = lib.smla_fwd_host_workspace_size
+    assert f(0, 16, 576, 512, 64, 0, 0) == 0
+    assert f(4, 0, 576, 512, 64, 0, 0) == 0
+    for T, h, topk, chunk in [(4, 16, 64, 0), (1000, 16, 2048, 64),
+                              (1000, 128, 2048, 0), (8192, 128, 2048, 512)]:
+        cdiv = lambda a, b: -(-a // b)
+        C = min(chunk, T) if chunk else min(T, max(256, cdiv(cdiv(T, 16), 64) * 64))
+        per_token = h * 576 * 2 + topk * 4 + 4 + h * 512 * 2 + h * 4
+        assert f(T, h, 576, 512, topk, 0, chunk) >= 2 * C * per_token, (T, h, chunk)
+    assert f(1000, 16, 576, 512, 2048, 0, 64) < f(1000, 16, 576, 512, 2048, 0, 512)
+
+
+def test_host_binding_rejects_bad_tensors_before_any_device_call(lib):
+    import torch
+    T, h, topk = 3, 16, 64
+    q = torch.zeros((T, h, 576), dtype=torch.bfloat16)
+    idx = torch.zeros((T, topk), dtype=torch.int32)
+    vl = torch.full((T,), topk, dtype=torch.int32)
+    kv = torch.zeros((256, 576), dtype=torch.bfloat16)
+    call = lambda **kw: smla.smla_fwd_host(
+        kw.get("q", q), kv, 0, None, kw.get("idx", idx), kw.get("vl", vl), 0.04)
+    with pytest.raises(ValueError, match="bf16"):
+        call(q=q.float())
+    with pytest.raises(ValueError, match="bf16"):
+        call(q=q.transpose(0, 1))
+    with pytest.raises(ValueError, match="int32"):
+        call(idx=idx.long())
+    with pytest.raises(ValueError, match="int32"):
+        call(idx=idx[:2])
+    with pytest.raises(ValueError, match="valid_len"):
+        call(vl=vl[:2])
+    with pytest.raises(ValueError, match="valid_len"):
+        call(vl=vl.long())
