@@ -115,7 +115,13 @@ typedef enum {
  *
  * Uses a library-owned device workspace for split partial results, grown
  * with cudaMalloc on first need (so the first call of a new, larger shape
- * allocates); smla_fwd_ws takes a caller-owned workspace instead.
+ * allocates, after waiting for the device to finish the work queued before);
+ * smla_fwd_ws takes a caller-owned workspace instead.  There is one such
+ * workspace per device: two calls that split their top-k ranges and may run
+ * at the same time on the GPU (different streams) race on it.  Keep such
+ * calls on one stream, or use smla_fwd_ws with one workspace per stream.
+ * Several host threads may call at once; calls that use this workspace are
+ * queued one at a time.
  */
 SMLA_API smla_status smla_fwd(const void* q, const void* kv_cache, int kv_dtype,
                      const float* k_scale, const int32_t* indices,

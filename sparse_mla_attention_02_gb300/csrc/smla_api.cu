@@ -128,11 +128,20 @@ smla_status run_fwd(const void* q, const void* kv, int kv_dtype,
     plan.split_len = topk;
     plan.workspace_bytes = 0;
   }
+  // The library-owned workspace is one buffer per device.  The lock is held
+  // from taking its address until the launches that use it are queued, so a
+  // call from another host thread cannot free it in between; a buffer that
+  // has to grow is freed only once the device has finished the work queued
+  // before (which may still read it).
+  std::unique_lock<std::mutex> ws_lock(g_mutex, std::defer_lock);
   if (plan.workspace_bytes > 0) {
     if (own_ws) {
-      std::lock_guard<std::mutex> lk(g_mutex);
+      ws_lock.lock();
       if (dev->workspace_bytes < plan.workspace_bytes) {
-        if (dev->workspace) cudaFree(dev->workspace);
+        if (dev->workspace) {
+          if (cudaDeviceSynchronize() != cudaSuccess) return SMLA_ERR_CUDA;
+          cudaFree(dev->workspace);
+        }
         dev->workspace = nullptr;
         dev->workspace_bytes = 0;
         if (cudaMalloc(&dev->workspace, plan.workspace_bytes) != cudaSuccess)
