@@ -108,35 +108,46 @@ def _check(code, what):
         raise SmlaError(code, what)
 
 
+def _require(cond, what):
+    """Argument check of the binding (kept under ``python -O``)."""
+    if not cond:
+        raise ValueError(what)
+
+
 def _kv_slots(kv_cache, kv_dtype, k_scale, d_qk, num_slots):
     """Check the cache and its scales; return the slot count."""
     import torch
-    assert kv_cache.is_cuda and kv_cache.is_contiguous()
+    _require(kv_cache.is_cuda and kv_cache.is_contiguous(),
+             "kv_cache must be a contiguous device tensor")
     if kv_dtype == SMLA_KV_BF16:
-        assert kv_cache.dtype == torch.bfloat16
+        _require(kv_cache.dtype == torch.bfloat16, "a bf16 cache must be torch.bfloat16")
     else:
-        assert kv_cache.dtype == torch.uint8
+        _require(kv_cache.dtype == torch.uint8, "an E4M3 cache must be torch.uint8 bytes")
     if kv_dtype in (SMLA_KV_FP8_E4M3, SMLA_KV_FP8_E4M3_GROUP128, SMLA_KV_FP8_E4M3_GROUP4_KPE):
-        assert k_scale is not None and k_scale.dtype == torch.float32
-        assert k_scale.is_cuda and k_scale.is_contiguous()
+        _require(k_scale is not None and k_scale.dtype == torch.float32 and
+                 k_scale.is_cuda and k_scale.is_contiguous(),
+                 "this cache format needs k_scale, a contiguous fp32 device tensor")
     row = DS_MLA_ROW_BYTES if kv_dtype == SMLA_KV_FP8_DS_MLA else d_qk
     return kv_cache.numel() // row if num_slots is None else int(num_slots)
 
 
 def _idx_checks(indices, valid_len, T):
     import torch
-    assert indices.is_cuda and indices.dtype == torch.int32
-    assert indices.is_contiguous() and indices.shape[0] == T
+    _require(indices.is_cuda and indices.dtype == torch.int32 and indices.is_contiguous()
+             and indices.dim() == 2 and indices.shape[0] == T,
+             "indices must be a contiguous int32 device tensor [T, topk]")
     if valid_len is not None:
-        assert valid_len.is_cuda and valid_len.dtype == torch.int32
-        assert valid_len.is_contiguous() and valid_len.shape == (T,)
+        _require(valid_len.is_cuda and valid_len.dtype == torch.int32 and
+                 valid_len.is_contiguous() and valid_len.shape == (T,),
+                 "valid_len must be a contiguous int32 device tensor [T]")
 
 
 def _in_args(q, kv_cache, kv_dtype, k_scale, indices, valid_len, sm_scale,
              num_slots):
     """The input arguments of the forward entry points, checked."""
     import torch
-    assert q.is_cuda and q.dtype == torch.bfloat16 and q.is_contiguous()
+    _require(q.is_cuda and q.dtype == torch.bfloat16 and q.is_contiguous() and q.dim() == 3,
+             "q must be a contiguous bf16 device tensor [T, h, d_qk]")
     T, h, d_qk = q.shape
     S = _kv_slots(kv_cache, kv_dtype, k_scale, d_qk, num_slots)
     _idx_checks(indices, valid_len, T)
@@ -147,7 +158,8 @@ def _in_args(q, kv_cache, kv_dtype, k_scale, indices, valid_len, sm_scale,
 def _fwd_args(q, kv_cache, kv_dtype, k_scale, indices, valid_len, sm_scale,
               out, lse, num_slots):
     import torch
-    assert q.is_cuda and q.dtype == torch.bfloat16 and q.is_contiguous()
+    _require(q.is_cuda and q.dtype == torch.bfloat16 and q.is_contiguous() and q.dim() == 3,
+             "q must be a contiguous bf16 device tensor [T, h, d_qk]")
     T, h, d_qk = q.shape
     S = _kv_slots(kv_cache, kv_dtype, k_scale, d_qk, num_slots)
     _idx_checks(indices, valid_len, T)
@@ -155,11 +167,11 @@ def _fwd_args(q, kv_cache, kv_dtype, k_scale, indices, valid_len, sm_scale,
     d_v = 512
     if out is None:
         out = torch.empty((T, h, d_v), dtype=torch.bfloat16, device=q.device)
-    assert out.dtype == torch.bfloat16 and out.is_contiguous()
-    assert out.shape == (T, h, d_v)
+    _require(out.dtype == torch.bfloat16 and out.is_contiguous() and out.shape == (T, h, d_v),
+             "out must be contiguous bf16 [T, h, 512]")
     if lse is not None:
-        assert lse.dtype == torch.float32 and lse.is_contiguous()
-        assert lse.shape == (T, h)
+        _require(lse.dtype == torch.float32 and lse.is_contiguous() and lse.shape == (T, h),
+                 "lse must be contiguous fp32 [T, h]")
     args = [_p(q), _p(kv_cache), int(kv_dtype), _p(k_scale), _p(indices),
             _p(valid_len), T, h, d_qk, d_v, topk, S, float(sm_scale),
             _p(out), _p(lse)]
@@ -192,23 +204,28 @@ def smla_fwd_split_q(q_nope, q_pe, kv_cache, kv_dtype, k_scale, indices, valid_l
     Returns (out bf16 [T,h,512], lse f32 [T,h] or None)."""
     import torch
     lib = load()
-    assert q_nope.is_cuda and q_nope.dtype == torch.bfloat16 and q_nope.is_contiguous()
+    _require(q_nope.is_cuda and q_nope.dtype == torch.bfloat16 and q_nope.is_contiguous(),
+             "q_nope must be a contiguous bf16 device tensor")
     if q_pe is None:
         T, h, d_qk = q_nope.shape
     else:
         T, h, d_nope = q_nope.shape
-        assert d_nope == 512 and q_pe.shape[:2] == (T, h)
-        assert q_pe.is_cuda and q_pe.dtype == torch.bfloat16 and q_pe.is_contiguous()
+        _require(d_nope == 512 and q_pe.shape[:2] == (T, h),
+                 "q_nope must be [T, h, 512] and q_pe [T, h, d_qk - 512]")
+        _require(q_pe.is_cuda and q_pe.dtype == torch.bfloat16 and q_pe.is_contiguous(),
+                 "q_pe must be a contiguous bf16 device tensor")
         d_qk = 512 + q_pe.shape[2]
     S = _kv_slots(kv_cache, kv_dtype, k_scale, d_qk, num_slots)
     _idx_checks(indices, valid_len, T)
     if out is None:
         out = torch.empty((T, h, 512), dtype=torch.bfloat16, device=q_nope.device)
-    assert out.dtype == torch.bfloat16 and out.is_contiguous() and out.shape == (T, h, 512)
+    _require(out.dtype == torch.bfloat16 and out.is_contiguous() and out.shape == (T, h, 512),
+             "out must be contiguous bf16 [T, h, 512]")
     if lse is None and want_lse:
         lse = torch.empty((T, h), dtype=torch.float32, device=q_nope.device)
     if lse is not None:
-        assert lse.dtype == torch.float32 and lse.is_contiguous() and lse.shape == (T, h)
+        _require(lse.dtype == torch.float32 and lse.is_contiguous() and lse.shape == (T, h),
+                 "lse must be contiguous fp32 [T, h]")
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.smla_fwd_split_q(_p(q_nope), _p(q_pe), _p(kv_cache), int(kv_dtype),
                                 _p(k_scale), float(kpe_scale), _p(indices), _p(valid_len),
@@ -230,12 +247,17 @@ def smla_cache_write_e4m3_group(kv_c, k_pe, slot_mapping, kv_cache, scales,
     N = kv_c.shape[0]
     for x in (kv_c, k_pe):
         if x is not None:
-            assert x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous()
-    assert kv_c.shape == (N, 512)
+            _require(x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous(),
+                     "kv_c and k_pe must be contiguous bf16 device tensors")
+    _require(kv_c.shape == (N, 512), "kv_c must be [N, 512]")
     d_qk = 512 if k_pe is None else 512 + k_pe.shape[1]
-    assert slot_mapping.dtype == torch.int32 and slot_mapping.shape == (N,)
-    assert kv_cache.dtype == torch.uint8 and kv_cache.shape[1] == d_qk
-    assert scales.dtype == torch.float32 and scales.shape == (kv_cache.shape[0], (d_qk + 127) // 128)
+    _require(slot_mapping.dtype == torch.int32 and slot_mapping.shape == (N,),
+             "slot_mapping must be int32 [N]")
+    _require(kv_cache.dtype == torch.uint8 and kv_cache.dim() == 2 and kv_cache.shape[1] == d_qk,
+             "kv_cache must be uint8 [S, d_qk]")
+    _require(scales.dtype == torch.float32 and
+             scales.shape == (kv_cache.shape[0], (d_qk + 127) // 128),
+             "scales must be fp32 [S, ceil(d_qk / 128)]")
     _check(lib.smla_cache_write_e4m3_group(_p(kv_c), _p(k_pe), _p(slot_mapping), N, d_qk,
                                            kv_cache.shape[0], _p(kv_cache), _p(scales),
                                            _stream(stream)), "smla_cache_write_e4m3_group")
@@ -253,8 +275,10 @@ def smla_fwd_partial(q, kv_cache, kv_dtype, k_scale, indices, valid_len,
         out = torch.empty((T, h, 512), dtype=torch.float32, device=q.device)
     if lse is None:
         lse = torch.empty((T, h), dtype=torch.float32, device=q.device)
-    assert out.dtype == torch.float32 and out.is_contiguous() and out.shape == (T, h, 512)
-    assert lse.dtype == torch.float32 and lse.is_contiguous() and lse.shape == (T, h)
+    _require(out.dtype == torch.float32 and out.is_contiguous() and out.shape == (T, h, 512),
+             "out must be contiguous fp32 [T, h, 512]")
+    _require(lse.dtype == torch.float32 and lse.is_contiguous() and lse.shape == (T, h),
+             "lse must be contiguous fp32 [T, h]")
     args = _in_args(q, kv_cache, kv_dtype, k_scale, indices, valid_len,
                     sm_scale, num_slots) + [_p(out), _p(lse)]
     _check(lib.smla_fwd_partial(*args, _stream(stream)), "smla_fwd_partial")
@@ -280,8 +304,10 @@ def smla_fwd_paged(q, kv_cache, kv_dtype, k_scale, token_indices, req_id,
     args, out, lse = _fwd_args(q, kv_cache, kv_dtype, k_scale, token_indices,
                                valid_len, sm_scale, out, lse, num_slots)
     for x in (req_id, block_table):
-        assert x.is_cuda and x.dtype == torch.int32 and x.is_contiguous()
-    assert req_id.shape == (args[6],) and block_table.dim() == 2
+        _require(x.is_cuda and x.dtype == torch.int32 and x.is_contiguous(),
+                 "req_id and block_table must be contiguous int32 device tensors")
+    _require(req_id.shape == (args[6],) and block_table.dim() == 2,
+             "req_id must be [T] and block_table [num_reqs, stride]")
     ws_p = None if workspace is None else _p(workspace)
     ws_n = 0 if workspace is None else workspace.numel()
     pargs = args[:4] + [args[4], _p(req_id), _p(block_table),
@@ -386,9 +412,10 @@ def smla_combine(o_parts, lse_parts, out=None, lse=None, stream=None):
     import torch
     lib = load()
     P, rows, d_v = o_parts.shape
-    assert o_parts.dtype == torch.float32 and o_parts.is_contiguous()
-    assert lse_parts.dtype == torch.float32 and lse_parts.is_contiguous()
-    assert lse_parts.shape == (P, rows)
+    _require(o_parts.dtype == torch.float32 and o_parts.is_contiguous(),
+             "o_parts must be contiguous fp32 [P, rows, 512]")
+    _require(lse_parts.dtype == torch.float32 and lse_parts.is_contiguous() and
+             lse_parts.shape == (P, rows), "lse_parts must be contiguous fp32 [P, rows]")
     if out is None:
         out = torch.empty((rows, d_v), dtype=torch.bfloat16, device=o_parts.device)
     if lse is None:

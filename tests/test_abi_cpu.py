@@ -247,3 +247,28 @@ def test_host_binding_rejects_bad_tensors_before_any_device_call(lib):
         call(vl=vl[:2])
     with pytest.raises(ValueError, match="valid_len"):
         call(vl=vl.long())
+
+
+def test_device_entry_points_refuse_host_tensors(lib):
+    """Host tensors given to a device entry point are refused by the binding
+    (a ValueError naming the argument) before any pointer reaches the
+    library; the checks survive ``python -O``."""
+    import torch
+    T, h, topk = 2, 16, 64
+    q = torch.zeros((T, h, 576), dtype=torch.bfloat16)
+    kv = torch.zeros((256, 576), dtype=torch.bfloat16)
+    idx = torch.zeros((T, topk), dtype=torch.int32)
+    with pytest.raises(ValueError, match="q must be"):
+        smla.smla_fwd(q, kv, 0, None, idx, None, 0.04)
+    with pytest.raises(ValueError, match="q must be"):
+        smla.smla_fwd_partial(q, kv, 0, None, idx, None, 0.04)
+    with pytest.raises(ValueError, match="q_nope must be"):
+        smla.smla_fwd_split_q(q, None, kv, 0, None, idx, None, 0.04)
+    with pytest.raises(ValueError, match="o_parts must be"):
+        smla.smla_combine(torch.zeros((2, 4, 512), dtype=torch.float64),
+                          torch.zeros((2, 4)))
+    with pytest.raises(ValueError, match="kv_c and k_pe"):
+        smla.smla_cache_write_e4m3_group(
+            torch.zeros((4, 512), dtype=torch.bfloat16), None,
+            torch.zeros(4, dtype=torch.int32), torch.zeros((8, 512), dtype=torch.uint8),
+            torch.zeros((8, 4)))
