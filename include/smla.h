@@ -159,6 +159,18 @@ SMLA_API smla_status smla_plan_info(int T, int h, int d_qk, int d_v, int topk,
                                     size_t* workspace_bytes);
 
 /*
+ * smla_plan_info_for — the same plan for a device with num_sms SMs, without
+ * querying any device: the kernel family, splits and workspace smla_fwd
+ * would choose there (for sizing workspaces ahead of time, on a host with
+ * or without a GPU).  smla_plan_info is this call with the current
+ * device's SM count.  Errors: those of smla_plan_info's shape checks, and
+ * SMLA_ERR_INVALID_ARG when num_sms < 1; never SMLA_ERR_CUDA.
+ */
+SMLA_API smla_status smla_plan_info_for(int T, int h, int d_qk, int d_v, int topk,
+                                        int kv_dtype, int num_sms, int* kernel,
+                                        int* splits, size_t* workspace_bytes);
+
+/*
  * smla_fwd_ws — smla_fwd with a caller-owned device workspace of at least
  * smla_workspace_size(...) bytes (256-byte aligned; NULL allowed when that
  * size is 0).  Returns SMLA_ERR_WORKSPACE if it is too small.  Performs no

@@ -80,6 +80,9 @@ def load():
         lib.smla_plan_info.argtypes = [I, I, I, I, I, I, ctypes.POINTER(I),
                                        ctypes.POINTER(I), ctypes.POINTER(SZ)]
         lib.smla_plan_info.restype = I
+        lib.smla_plan_info_for.argtypes = [I, I, I, I, I, I, I, ctypes.POINTER(I),
+                                           ctypes.POINTER(I), ctypes.POINTER(SZ)]
+        lib.smla_plan_info_for.restype = I
         lib.smla_combine.argtypes = [P, P, I, I64, I, P, P, P]
         lib.smla_combine.restype = I
         lib.smla_get_device_status.argtypes = [ctypes.POINTER(I), I]
@@ -332,6 +335,17 @@ def smla_plan_info(T, h, d_qk, topk, kv_dtype, d_v=512) -> dict:
     k, s, n = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_size_t(0)
     _check(lib.smla_plan_info(T, h, d_qk, d_v, topk, kv_dtype, ctypes.byref(k),
                               ctypes.byref(s), ctypes.byref(n)), "smla_plan_info")
+    return {"kernel": KERNEL_NAMES[k.value], "splits": s.value,
+            "workspace_bytes": n.value}
+
+
+def smla_plan_info_for(T, h, d_qk, topk, kv_dtype, num_sms, d_v=512) -> dict:
+    """``smla_plan_info_for``: the same plan for a device with ``num_sms``
+    SMs, without a device query (works on a host without a GPU)."""
+    lib = load()
+    k, s, n = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_size_t(0)
+    _check(lib.smla_plan_info_for(T, h, d_qk, d_v, topk, kv_dtype, num_sms, ctypes.byref(k),
+                                  ctypes.byref(s), ctypes.byref(n)), "smla_plan_info_for")
     return {"kernel": KERNEL_NAMES[k.value], "splits": s.value,
             "workspace_bytes": n.value}
 

@@ -377,22 +377,16 @@ size_t smla_workspace_size(int T, int h, int d_qk, int d_v, int topk,
       .workspace_bytes;
 }
 
-smla_status smla_plan_info(int T, int h, int d_qk, int d_v, int topk,
-                           int kv_dtype, int* kernel, int* splits,
-                           size_t* workspace_bytes) {
-  if (T < 1 || h < 1 || topk < 1) return SMLA_ERR_INVALID_ARG;
+smla_status smla_plan_info_for(int T, int h, int d_qk, int d_v, int topk,
+                               int kv_dtype, int num_sms, int* kernel, int* splits,
+                               size_t* workspace_bytes) {
+  if (T < 1 || h < 1 || topk < 1 || num_sms < 1) return SMLA_ERR_INVALID_ARG;
   if (h > 128 || (d_qk != 512 && d_qk != 576) || d_v != 512 ||
       kv_dtype < SMLA_KV_BF16 || kv_dtype > SMLA_KV_FP8_E4M3_GROUP4_KPE ||
       ((kv_dtype == SMLA_KV_FP8_DS_MLA || kv_dtype == SMLA_KV_FP8_E4M3_GROUP4_KPE) &&
        d_qk != 576))
     return SMLA_ERR_UNSUPPORTED;
-  DeviceInfo* dev = nullptr;
-  {
-    std::lock_guard<std::mutex> lk(g_mutex);
-    const smla_status st = device_info(&dev);
-    if (st != SMLA_OK) return st;
-  }
-  const smla::Plan pl = smla::make_plan(T, h, d_qk, d_v, topk, kv_dtype, dev->num_sms);
+  const smla::Plan pl = smla::make_plan(T, h, d_qk, d_v, topk, kv_dtype, num_sms);
   if (kernel)
     *kernel = pl.kind == smla::kKernelTcKeys ? SMLA_KERNEL_TC_KEYS
               : pl.kind == smla::kKernelTc   ? SMLA_KERNEL_TC_HEADS
@@ -400,6 +394,22 @@ smla_status smla_plan_info(int T, int h, int d_qk, int d_v, int topk,
   if (splits) *splits = pl.splits;
   if (workspace_bytes) *workspace_bytes = pl.workspace_bytes;
   return SMLA_OK;
+}
+
+smla_status smla_plan_info(int T, int h, int d_qk, int d_v, int topk,
+                           int kv_dtype, int* kernel, int* splits,
+                           size_t* workspace_bytes) {
+  // Shape errors first, without a device query.
+  smla_status st = smla_plan_info_for(T, h, d_qk, d_v, topk, kv_dtype, 1, nullptr,
+                                      nullptr, nullptr);
+  if (st != SMLA_OK) return st;
+  DeviceInfo* dev = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    if ((st = device_info(&dev)) != SMLA_OK) return st;
+  }
+  return smla_plan_info_for(T, h, d_qk, d_v, topk, kv_dtype, dev->num_sms, kernel, splits,
+                            workspace_bytes);
 }
 
 smla_status smla_combine(const float* o_parts, const float* lse_parts,
