@@ -33,6 +33,13 @@ def test_dispatch_uses_keys_kernel_up_to_16_heads(cuda_lib):
     assert cuda_lib.smla_plan_info(512, 16, 576, 4096, 2)["splits"] >= 2
 
 
+def test_device_plan_is_the_plan_for_its_sm_count(cuda_lib):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for shape in [(8192, 128, 576, 2048, 0), (64, 128, 576, 2048, 0), (2, 16, 576, 2048, 2),
+                  (80, 16, 576, 3000, 2), (4, 32, 576, 2048, 2), (128, 64, 512, 2048, 1)]:
+        assert cuda_lib.smla_plan_info(*shape) == cuda_lib.smla_plan_info_for(*shape, num_sms=sms)
+
+
 @pytest.mark.parametrize("kv_dtype", [0, 1, 2])
 @pytest.mark.parametrize("d_qk", [576, 512])
 @pytest.mark.parametrize("h", [1, 5, 16])
