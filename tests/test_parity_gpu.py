@@ -177,6 +177,17 @@ def test_fp8_decode_every_code_exactly(cuda_lib, h):
     compare(O, L, Or, Lr, "fp8_codes")
 
 
+@pytest.mark.parametrize("kv_dtype,h", [(0, 128), (1, 64), (0, 16), (2, 16)])
+def test_model_softmax_scale(cuda_lib, kv_dtype, h):
+    """sm_scale = 192**-0.5, the model's scale on the "Sparse MLA on Hopper"
+    compare page (CutlassFA3MLASparseImpl.__init__ comment; SOFTMAX_SCALE of
+    the FlashMLA fallback test): about 1.7x 1/sqrt(576), a peakier softmax."""
+    w = W.custom(T=6, h=h, topk=300, num_slots=1000, kv_dtype=kv_dtype,
+                 valid=[300, 299, 150, 49, 48, 1], sm_scale=192 ** -0.5,
+                 seed=270 + h + kv_dtype)
+    check(cuda_lib, w)
+
+
 def test_duplicate_indices(cuda_lib):
     w = W.custom(T=4, h=16, topk=64, num_slots=20, valid=[64, 30, 5, 1],
                  seed=37, distinct=False, name="duplicates")
