@@ -23,7 +23,6 @@ import argparse
 import hashlib
 import glob
 import json
-import math
 import os
 import statistics
 import subprocess

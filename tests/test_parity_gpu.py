@@ -12,14 +12,13 @@ batch) plus the degenerate cases of the method (valid = 0, all masked,
 scattered -1, out-of-range ids, duplicates, h not a multiple of 16, topk not a
 multiple of the block, NULL valid_len).
 """
-import math
 
 import numpy as np
 import pytest
 import torch
 
 from sparse_mla_attention_02_gb300 import workloads as W
-from tests._helpers import bits16, kv_numpy, oracle_fwd
+from tests._helpers import oracle_fwd
 
 import oracle
 
