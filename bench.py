@@ -41,6 +41,7 @@ from sparse_mla_attention_02_gb300 import workloads as W  # noqa: E402
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
                   "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 1024 * 1024
+FLUSH_BYTES = 256 * 1024 * 1024     # written between cold-L2 steps (> L2)
 METRIC = ("sparse MLA fwd TFLOP/s & query-tokens/s at h=128 topk=2048; "
           "% of roofline")
 
@@ -181,7 +182,8 @@ def job_throughput(units_per_rank: float, world: int, steps: int, t_max: float) 
 
 
 def time_steps(fn, steps, stream):
-    """K steps back to back on `stream`, timed with CUDA events there."""
+    """K steps back to back on `stream`, timed with CUDA events there (a
+    step may find its inputs in L2 from the step before: warm L2)."""
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     start.record(stream)
@@ -190,6 +192,23 @@ def time_steps(fn, steps, stream):
     end.record(stream)
     end.synchronize()
     return start.elapsed_time(end) / 1e3
+
+
+def time_steps_cold(fn, steps, stream, flush):
+    """K steps, each after `flush` (a buffer larger than L2) was written on
+    `stream`, so that every step starts with a cold L2; each step alone is
+    timed with CUDA events on `stream` (the flush is outside), and the times
+    are summed."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+    evs[-1][1].synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs) / 1e3
 
 
 def run_ours(args, rank, world, local_rank):
@@ -244,6 +263,8 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize(dev)
     barrier()
     clocks = cs.summary()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    cold_el = ranks_max(time_steps_cold(f, args.steps, stream, flush))
     t_max = ranks_max(elapsed)
     ms = 1e3 * t_max / args.steps
     launches_per_step = 1 + (1 if ws_n > 0 else 0)
@@ -264,6 +285,7 @@ def run_ours(args, rank, world, local_rank):
         "algorithmic_bytes_per_launch": {"U": U, "G": G},
     }
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["ms_per_step_cold_l2"] = round(1e3 * cold_el / args.steps, 4)
     roof["frac_of_sustained"] = round(achieved / pk["bf16_tflops_sustained"], 4) \
         if bound_tensor else None
 
@@ -271,7 +293,11 @@ def run_ours(args, rank, world, local_rank):
         if rank == 0:
             print(json.dumps({"config": args.config, "T": w.T,
                               "ms_per_step": round(ms, 4),
+                              "ms_per_step_cold_l2": round(1e3 * cold_el / args.steps, 4),
                               "tflops": round(value, 3),
+                              "gbs_G": round(G / (elapsed / args.steps) / 1e9, 1),
+                              "kernel": smla.smla_plan_info(w.T, w.h, w.d_qk, w.topk,
+                                                            w.kv_dtype)["kernel"],
                               "flops_per_launch": fl, "U": U, "G": G}), flush=True)
         return
 
@@ -336,21 +362,32 @@ def run_ours(args, rank, world, local_rank):
             barrier()
             k2 = max(args.steps, 20) if name != "mixed_fp8_group" else max(3, args.steps)
             el2 = ranks_max(time_steps(f2, k2, stream))
+            cold2 = ranks_max(time_steps_cold(f2, k2, stream, flush))
             fl2 = flops_of(w2)
             U2, G2 = bytes_model(w2)
-            t2 = el2 / k2
+            t2, tc2 = el2 / k2, cold2 / k2
+            roof2 = max(fl2 / (pk["bf16_tflops"] * 1e12), U2 / (pk["hbm_gbs"] * 1e9))
             secondary[name] = {
                 "tflops": round(world * fl2 / t2 / 1e12, 3),
                 "tokens_per_s": round(world * w2.T / t2, 1),
                 "ms_per_step": round(1e3 * t2, 4),
+                "ms_per_step_cold_l2": round(1e3 * tc2, 4),
                 "hbm_gbs_U": round(U2 / t2 / 1e9, 1),
                 "frac_hbm_U": round(U2 / t2 / 1e9 / pk["hbm_gbs"], 4),
-                "roofline_frac": round(max(fl2 / (pk["bf16_tflops"] * 1e12),
-                                           U2 / (pk["hbm_gbs"] * 1e9)) / t2, 4),
+                "roofline_frac": round(roof2 / t2, 4),
+                "roofline_frac_cold_l2": round(roof2 / tc2, 4),
+                # gathered bytes (every selected row once per token) per second
+                "hbm_gbs_G": round(G2 / t2 / 1e9, 1),
+                "frac_hbm_G": round(G2 / t2 / 1e9 / pk["hbm_gbs"], 4),
+                "frac_hbm_G_cold_l2": round(G2 / tc2 / 1e9 / pk["hbm_gbs"], 4),
+                "bytes_per_launch": {"U": U2, "G": G2},
+                "traffic": ncu_traffic(name),
                 "splits_workspace_bytes": n2,
                 "kernel": smla.smla_plan_info(w2.T, w2.h, w2.d_qk, w2.topk,
                                               w2.kv_dtype)["kernel"],
             }
+            if rank == 0 and world == 1 and not args.no_cpu:
+                secondary[name]["cpu_baseline"] = cpu_baseline(w2, args.cpu_seconds / 3)
             if name == "bf16_decode":
                 # The same decode step on request-local positions through
                 # smla_fwd_paged: request r's 32768-slot context as 512
@@ -420,6 +457,7 @@ def run_ours(args, rank, world, local_rank):
         }
         del kv_c, k_pe, slots, cache, scales
         torch.cuda.empty_cache()
+    del flush
 
     if rank == 0:
         line = {
@@ -526,8 +564,9 @@ def run_reference(args, rank, world):
         "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": f"{args.config}: T=8192 h=128 d_qk=576 d_v=512 "
-                               "topk=2048 (token sample, see cpu_baseline)"},
+        "config": {"workload": f"{args.config}: T={T} h={w.h} d_qk={w.d_qk} "
+                               f"d_v={w.d_v} topk={w.topk} (token sample, see "
+                               "cpu_baseline)"},
         "tokens_per_s": round(len(sel) * args.steps / dt, 3),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s",
                          "cores": cores, "kind": "oracle", "sample": sample},
@@ -535,6 +574,27 @@ def run_reference(args, rank, world):
                 "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def spawn_ranks(args) -> int:
+    """--gpus N > 1 without a launcher: start N ranks (one per GPU) with
+    torch.distributed.run on this node and return its exit code; refuse when
+    fewer than N GPUs are visible (never report fewer GPUs than asked)."""
+    if args.impl == "ours":
+        n = torch.cuda.device_count()
+        if n < args.gpus:
+            print(f"bench.py: --gpus {args.gpus} requested, {n} GPU(s) visible",
+                  file=sys.stderr)
+            return 2
+    import socket
+    sk = socket.socket()
+    sk.bind(("127.0.0.1", 0))
+    port = sk.getsockname()[1]
+    sk.close()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={args.gpus}", "--master-addr", "127.0.0.1",
+           "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd)
 
 
 def main():
@@ -555,8 +615,13 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        sys.exit(spawn_ranks(args))
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
+        sys.exit(2)
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist

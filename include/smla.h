@@ -141,7 +141,10 @@ SMLA_API size_t smla_workspace_size(int T, int h, int d_qk, int d_v, int topk,
 typedef enum {
   SMLA_KERNEL_CUDA_CORE = 0,     /* fp32 CUDA-core kernel (any supported shape) */
   SMLA_KERNEL_TC_HEADS = 1,      /* tcgen05, heads as the MMA rows (h <= 128) */
-  SMLA_KERNEL_TC_KEYS = 2        /* tcgen05, top-k positions as the MMA rows (h <= 16) */
+  SMLA_KERNEL_TC_KEYS = 2,       /* tcgen05, top-k positions as the MMA rows (bf16, h <= 16) */
+  SMLA_KERNEL_TC_KEYS_FP8 = 3    /* tcgen05 with E4M3 operands, top-k positions as the MMA
+                                    rows, heads in groups of 16 (E4M3 caches: every layout
+                                    with group scales, any h; one scale per tensor, h <= 16) */
 } smla_kernel;
 
 /*
@@ -401,6 +404,29 @@ SMLA_API smla_status smla_fwd_noalloc(const void* q, const void* kv_cache,
  * and diagnostics, not the hot path.
  */
 SMLA_API smla_status smla_get_device_status(int* status_out, int clear);
+
+/*
+ * smla_test_set_stall — for tests of the timeout path only (no counterpart on
+ * the pages).  Every wait inside the tensor-core kernels is bounded: a wait
+ * that runs out sets SMLA_ERR_TIMEOUT in the device status word, the block
+ * drains the copies and MMAs it started, frees its tensor memory and
+ * returns, and the launch's outputs are undefined.  This switch lets a test
+ * reach that path without a fault or a hang.
+ *
+ *  stall          nonzero: later tensor-core launches on the current device
+ *                 leave out the first batch of score MMAs of every work
+ *                 unit, so the wait for those scores cannot complete and
+ *                 runs out; 0: normal launches.
+ *  wait_limit_us  the time limit of one bounded wait in later launches on
+ *                 the current device, in microseconds; 0 = the default
+ *                 (500 ms).
+ * The setting is process-wide per device and applies to launches made after
+ * the call; it does not touch the status word (smla_get_device_status clears
+ * it).  A timeout of one launch does not abort later launches.  Returns
+ * SMLA_ERR_INVALID_ARG for wait_limit_us < 0, SMLA_ERR_CUDA when the device
+ * cannot be queried.
+ */
+SMLA_API smla_status smla_test_set_stall(int stall, int wait_limit_us);
 
 /* smla_status_string — a static, human-readable name for a status code. */
 SMLA_API const char* smla_status_string(int status);

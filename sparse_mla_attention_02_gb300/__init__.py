@@ -87,6 +87,8 @@ def load():
         lib.smla_combine.restype = I
         lib.smla_get_device_status.argtypes = [ctypes.POINTER(I), I]
         lib.smla_get_device_status.restype = I
+        lib.smla_test_set_stall.argtypes = [I, I]
+        lib.smla_test_set_stall.restype = I
         lib.smla_status_string.argtypes = [I]
         lib.smla_status_string.restype = ctypes.c_char_p
         lib.smla_version.argtypes = []
@@ -325,7 +327,7 @@ def smla_workspace_size(T, h, d_qk, topk, kv_dtype, d_v=512) -> int:
     return int(load().smla_workspace_size(T, h, d_qk, d_v, topk, kv_dtype))
 
 
-KERNEL_NAMES = {0: "cuda_core", 1: "tc_heads", 2: "tc_keys"}
+KERNEL_NAMES = {0: "cuda_core", 1: "tc_heads", 2: "tc_keys", 3: "tc_keys_fp8"}
 
 
 def smla_plan_info(T, h, d_qk, topk, kv_dtype, d_v=512) -> dict:
@@ -444,6 +446,15 @@ def smla_get_device_status(clear=True) -> int:
     _check(load().smla_get_device_status(ctypes.byref(v), int(clear)),
            "smla_get_device_status")
     return v.value
+
+
+def smla_test_set_stall(stall: bool, wait_limit_us: int = 0) -> None:
+    """Tests of the timeout path only: while ``stall`` is set, tensor-core
+    launches on the current device leave out each unit's first batch of
+    score MMAs, so a bounded wait runs out after ``wait_limit_us`` (0 = the
+    default limit) and the launch reports SMLA_ERR_TIMEOUT."""
+    _check(load().smla_test_set_stall(int(bool(stall)), int(wait_limit_us)),
+           "smla_test_set_stall")
 
 
 def smla_status_string(code: int) -> str:

@@ -16,6 +16,9 @@
 namespace {
 
 __device__ int g_smla_status = 0;  // device status word (first error wins)
+// Bumped by every bounded wait that gives up; a launch's blocks compare it
+// with its value when they started (never reset).
+__device__ int g_smla_abort = 0;
 
 constexpr int kMaxDevices = 64;
 
@@ -23,6 +26,9 @@ struct DeviceInfo {
   bool ready = false;
   int num_sms = 0;
   int* status = nullptr;      // device address of g_smla_status
+  int* abort_ctr = nullptr;   // device address of g_smla_abort
+  int stall = 0;              // smla_test_set_stall
+  uint64_t wait_limit_ns = 0; // 0: the default limit
   void* workspace = nullptr;  // library-owned workspace for smla_fwd
   size_t workspace_bytes = 0;
 };
@@ -42,10 +48,13 @@ smla_status device_info(DeviceInfo** out) {
         cudaSuccess)
       return SMLA_ERR_CUDA;
     void* st = nullptr;
-    if (cudaGetSymbolAddress(&st, g_smla_status) != cudaSuccess)
+    void* ab = nullptr;
+    if (cudaGetSymbolAddress(&st, g_smla_status) != cudaSuccess ||
+        cudaGetSymbolAddress(&ab, g_smla_abort) != cudaSuccess)
       return SMLA_ERR_CUDA;
     d.num_sms = sms;
     d.status = static_cast<int*>(st);
+    d.abort_ctr = static_cast<int*>(ab);
     d.ready = true;
   }
   *out = &d;
@@ -110,9 +119,13 @@ smla_status run_fwd(const void* q, const void* kv, int kv_dtype,
   if ((valid_len && !aligned(valid_len, 4)) || (lse && !aligned(lse, 4)))
     return SMLA_ERR_INVALID_ARG;
   DeviceInfo* dev = nullptr;
+  int stall = 0;
+  uint64_t wait_limit_ns = smla::kWaitLimitNs;
   {
     std::lock_guard<std::mutex> lk(g_mutex);
     if ((st = device_info(&dev)) != SMLA_OK) return st;
+    stall = dev->stall;
+    if (dev->wait_limit_ns) wait_limit_ns = dev->wait_limit_ns;
   }
   smla::Plan plan =
       smla::make_plan(T, h, d_qk, d_v, topk, kv_dtype, dev->num_sms);
@@ -120,9 +133,7 @@ smla_status run_fwd(const void* q, const void* kv, int kv_dtype,
     // Partial-output mode: one range per token, written straight to the
     // caller's fp32 buffers (no workspace, no combine).  A top-k longer than
     // one range of the chosen kernel would need a split: not served.
-    if (plan.kind != smla::kKernelSimt && topk > (plan.kind == smla::kKernelTcKeys
-                                                      ? smla::tc_keys_max_range()
-                                                      : smla::tc_max_range()))
+    if (plan.kind != smla::kKernelSimt && topk > smla::plan_max_range(plan.kind))
       return SMLA_ERR_UNSUPPORTED;
     plan.splits = 1;
     plan.split_len = topk;
@@ -165,6 +176,9 @@ smla_status run_fwd(const void* q, const void* kv, int kv_dtype,
   p.out = out;
   p.lse = lse;
   p.status = dev->status;
+  p.abort_ctr = dev->abort_ctr;
+  p.wait_limit_ns = wait_limit_ns;
+  p.inject_stall = stall;
   p.num_slots = num_slots;
   p.kv_format = kv_dtype;
   p.T = T;
@@ -190,9 +204,10 @@ smla_status run_fwd(const void* q, const void* kv, int kv_dtype,
     p.o_part = static_cast<float*>(ws);
     p.lse_part = p.o_part + (size_t)plan.splits * T * h * d_v;
   }
-  const cudaError_t le = plan.kind == smla::kKernelTcKeys ? smla::launch_tc_keys(p, stream)
-                         : plan.kind == smla::kKernelTc   ? smla::launch_tc(p, stream)
-                                                          : smla::launch_simt(p, stream);
+  const cudaError_t le = plan.kind == smla::kKernelTcFp8    ? smla::launch_tc_fp8(p, stream)
+                         : plan.kind == smla::kKernelTcKeys ? smla::launch_tc_keys(p, stream)
+                         : plan.kind == smla::kKernelTc     ? smla::launch_tc(p, stream)
+                                                            : smla::launch_simt(p, stream);
   if (le != cudaSuccess) return SMLA_ERR_CUDA;
   if (plan.splits > 1) {
     if (smla::launch_combine(p.o_part, p.lse_part, plan.splits, (int64_t)T * h,
@@ -206,28 +221,54 @@ smla_status run_fwd(const void* q, const void* kv, int kv_dtype,
 
 namespace smla {
 
+int check_fwd_args_code(const void* q, const void* kv, int kv_dtype, const float* k_scale,
+                        const int32_t* indices, const int32_t* valid_len, int T, int h,
+                        int d_qk, int d_v, int topk, int64_t num_slots, const void* out,
+                        const float* lse) {
+  const smla_status st =
+      check_args(q, kv, kv_dtype, k_scale, indices, T, h, d_qk, d_v, topk, num_slots, out);
+  if (st != SMLA_OK || T == 0) return st;
+  if ((valid_len && !aligned(valid_len, 4)) || (lse && !aligned(lse, 4)))
+    return SMLA_ERR_INVALID_ARG;
+  return SMLA_OK;
+}
+
+int plan_max_range(int kind) {
+  return kind == kKernelTcFp8    ? tc_fp8_max_range()
+         : kind == kKernelTcKeys ? tc_keys_max_range()
+                                 : tc_max_range();
+}
+
 // Split plan.  Valid counts are device data, so ranges are cut over topk; a
 // range past a token's valid count yields an empty partial (0, -inf) that the
 // combine ignores.
-//  - tensor-core paths: one unit = (token, range) on one CTA per SM
-//    (keys-major, h <= 16) or on a 2-SM cluster (heads-major, up to 128
-//    heads); split only when the tokens alone leave more than half of the
-//    SMs (or SM pairs) idle (each split costs partial-O traffic), or when
-//    topk is longer than one unit's range.
+//  - kernel family: E4M3 caches with per-(slot, group) scales (every layout)
+//    and per-tensor E4M3 with h <= 16 run on the E4M3-operand keys-major
+//    kernel (one CTA per token, range and group of 16 heads); bf16 with
+//    h <= 16 on the bf16 keys-major kernel (one CTA per unit); bf16 and
+//    per-tensor E4M3 with more heads on the heads-major kernel (a 2-SM
+//    cluster per unit, up to 128 heads).
+//  - tensor-core paths: split only when the units alone leave more than half
+//    of the SMs (or SM pairs) idle (each split costs partial-O traffic), or
+//    when topk is longer than one unit's range.
 //  - CUDA-core path: enough (token, 16-head group, range) units to fill every
 //    SM twice.
 Plan make_plan(int T, int h, int d_qk, int d_v, int topk, int kv_format,
                int num_sms) {
   Plan pl{};
   int splits = 1, gran = 32;
-  const bool keys = tc_keys_supported(h, d_qk, kv_format);
-  if (keys || tc_supported(h, d_qk, kv_format)) {
-    pl.kind = keys ? kKernelTcKeys : kKernelTc;
-    gran = 64;
-    const int max_range = keys ? tc_keys_max_range() : tc_max_range();
-    const int places = keys ? (num_sms > 0 ? num_sms : 1) : (num_sms > 1 ? num_sms / 2 : 1);
-    if (2LL * T < places) {
-      splits = places / (T > 0 ? T : 1);
+  const bool fp8 = tc_fp8_supported(h, d_qk, kv_format) && (kv_format != kE4m3 || h <= 16);
+  const bool keys = !fp8 && tc_keys_supported(h, d_qk, kv_format);
+  if (fp8 || keys || tc_supported(h, d_qk, kv_format)) {
+    pl.kind = fp8 ? kKernelTcFp8 : keys ? kKernelTcKeys : kKernelTc;
+    gran = fp8 ? 128 : 64;
+    const int max_range = plan_max_range(pl.kind);
+    // units per (token, range): head groups of 16 for the E4M3-operand kernel
+    const int64_t per_token = fp8 ? (h + 15) / 16 : 1;
+    const int places = (fp8 || keys) ? (num_sms > 0 ? num_sms : 1)
+                                     : (num_sms > 1 ? num_sms / 2 : 1);
+    if (2LL * T * per_token < places) {
+      splits = (int)(places / ((T > 0 ? T : 1) * per_token));
       const int max_by_topk = (topk + 127) / 128;
       if (splits > max_by_topk) splits = max_by_topk;
       if (splits > 16) splits = 16;
@@ -388,9 +429,10 @@ smla_status smla_plan_info_for(int T, int h, int d_qk, int d_v, int topk,
     return SMLA_ERR_UNSUPPORTED;
   const smla::Plan pl = smla::make_plan(T, h, d_qk, d_v, topk, kv_dtype, num_sms);
   if (kernel)
-    *kernel = pl.kind == smla::kKernelTcKeys ? SMLA_KERNEL_TC_KEYS
-              : pl.kind == smla::kKernelTc   ? SMLA_KERNEL_TC_HEADS
-                                             : SMLA_KERNEL_CUDA_CORE;
+    *kernel = pl.kind == smla::kKernelTcFp8    ? SMLA_KERNEL_TC_KEYS_FP8
+              : pl.kind == smla::kKernelTcKeys ? SMLA_KERNEL_TC_KEYS
+              : pl.kind == smla::kKernelTc     ? SMLA_KERNEL_TC_HEADS
+                                               : SMLA_KERNEL_CUDA_CORE;
   if (splits) *splits = pl.splits;
   if (workspace_bytes) *workspace_bytes = pl.workspace_bytes;
   return SMLA_OK;
@@ -425,6 +467,17 @@ smla_status smla_combine(const float* o_parts, const float* lse_parts,
   if (smla::launch_combine(o_parts, lse_parts, n_parts, rows, d_v, out, lse,
                            stream) != cudaSuccess)
     return SMLA_ERR_CUDA;
+  return SMLA_OK;
+}
+
+smla_status smla_test_set_stall(int stall, int wait_limit_us) {
+  if (wait_limit_us < 0) return SMLA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mutex);
+  DeviceInfo* dev = nullptr;
+  const smla_status st = device_info(&dev);
+  if (st != SMLA_OK) return st;
+  dev->stall = stall ? 1 : 0;
+  dev->wait_limit_ns = (uint64_t)wait_limit_us * 1000ull;
   return SMLA_OK;
 }
 

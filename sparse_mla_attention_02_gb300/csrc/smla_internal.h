@@ -34,6 +34,10 @@ struct FwdParams {
   float* o_part;          // split partials [splits, T, h, d_v] (splits > 1)
   float* lse_part;        // [splits, T, h]
   int* status;            // device status word
+  int* abort_ctr;         // device abort counter (bounded waits, see Waiter)
+  uint64_t wait_limit_ns; // time limit of one bounded wait
+  int inject_stall;       // tests only: the first QK batch of every unit is
+                          // not issued, so the wait for its scores runs out
   int64_t num_slots;
   int kv_format;
   int T, h, d_qk, d_v, topk;
@@ -102,7 +106,7 @@ __device__ __forceinline__ int token_req(const FwdParams& p, int t, bool& bad) {
 #endif
 
 // Which kernel family a plan uses.
-enum KernelKind { kKernelSimt = 0, kKernelTc = 1, kKernelTcKeys = 2 };
+enum KernelKind { kKernelSimt = 0, kKernelTc = 1, kKernelTcKeys = 2, kKernelTcFp8 = 3 };
 
 struct Plan {
   int kind;
@@ -111,6 +115,18 @@ struct Plan {
   size_t workspace_bytes;   // partial O and LSE for splits > 1, else 0
   int lpt;                  // longest-first unit order (see FwdParams::lpt)
 };
+
+// Largest top-k range one unit of a tensor-core kernel family covers.
+int plan_max_range(int kind);
+
+// Default time limit of one bounded wait in the tensor-core kernels.
+constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;
+
+// The host-side argument checks of smla_fwd (codes as smla_status).
+int check_fwd_args_code(const void* q, const void* kv, int kv_dtype, const float* k_scale,
+                        const int32_t* indices, const int32_t* valid_len, int T, int h,
+                        int d_qk, int d_v, int topk, int64_t num_slots, const void* out,
+                        const float* lse);
 
 Plan make_plan(int T, int h, int d_qk, int d_v, int topk, int kv_format,
                int num_sms);
@@ -123,6 +139,11 @@ cudaError_t launch_tc(const FwdParams& p, cudaStream_t stream);
 bool tc_keys_supported(int h, int d_qk, int kv_format);
 int tc_keys_max_range();
 cudaError_t launch_tc_keys(const FwdParams& p, cudaStream_t stream);
+// Keys-major tensor-core kernel with E4M3 operands (every E4M3 format, any
+// h in groups of 16 heads).
+bool tc_fp8_supported(int h, int d_qk, int kv_format);
+int tc_fp8_max_range();
+cudaError_t launch_tc_fp8(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_cache_write(const void* kv_c, const void* k_pe, const int32_t* slot,
                                int N, int d_qk, int64_t num_slots, void* cache,
                                float* scales, int* status, cudaStream_t stream);

@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "../../include/smla.h"
+#include "smla_internal.h"
 
 namespace {
 
@@ -48,6 +49,12 @@ extern "C" SMLA_API smla_status smla_fwd_noalloc(
     return smla_fwd_ws(q, kv_cache, kv_dtype, k_scale, indices, valid_len, T,
                        h, d_qk, d_v, topk, num_slots, sm_scale, out, lse,
                        nullptr, 0, stream);
+  // smla_fwd's own argument checks first, so that a shape or argument that
+  // smla_fwd rejects gets the same code here.
+  const int chk = smla::check_fwd_args_code(q, kv_cache, kv_dtype, k_scale, indices,
+                                            valid_len, T, h, d_qk, d_v, topk, num_slots,
+                                            out, lse);
+  if (chk != SMLA_OK) return (smla_status)chk;
   void* scratch = scratch_on_current_device();
   if (!scratch) return SMLA_ERR_CUDA;
   // The split plan's need for this shape; larger than the fixed array means

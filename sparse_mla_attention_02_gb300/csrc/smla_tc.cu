@@ -113,6 +113,7 @@ enum {
   kBarQReady,
   kBarQStaged,                         // the staged Q rows have been read
   kBarQLoaded,                         // the Q boxes have landed (TMA staging)
+  kBarDrain,                           // teardown: the MMA warp's MMAs are done
   kNumBars
 };
 constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
@@ -173,7 +174,7 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
 
   auto bar = [&](int i) { return sb + kOffBar + 8u * (uint32_t)i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffAbort);
-  Waiter W{abort_flag, p.status};
+  Waiter W = make_waiter(abort_flag, p);
 
   // Q half, first step (bf16 caches): the 256 softmax threads copy the
   // CTA's Q half (128 heads x 2 * ksteps 16-byte pieces) into the staging
@@ -224,6 +225,7 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
     mbar_init(bar(kBarQReady), 256);
     mbar_init(bar(kBarQStaged), 256);
     mbar_init(bar(kBarQLoaded), 1);
+    mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0;
     fence_mbar_init_cluster();
     if (a.q_tma) {
@@ -282,6 +284,7 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
       W.wait(bar(kBarQReady), 0);
       tc_fence_after();
       auto issue_qk = [&](int j) {
+        if (p.inject_stall && j == 0) return;   // tests: block 0's scores never arrive
         const int s = j % kStages;
         W.wait(bar(kBarKvFull + s), (j / kStages) & 1);
         if (j >= 2) W.wait(bar(kBarSEmpty + (j & 1)), ((j >> 1) - 1) & 1);
@@ -329,6 +332,12 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
         issue_pv(j);
       }
     }
+    // Every MMA this warp issued has completed (also after an abort) before
+    // the TMEM is freed and the tiles are left.
+    __syncwarp();
+    if (elect_one()) mma_commit(bar(kBarDrain));
+    __syncwarp();
+    W.drain(bar(kBarDrain), 0);
   } else if (warp < 4) {
     // ---- producers: a2 gather with TMA (tile::gather4) ----------------------
     // Per block: 12 groups of 4 rows x n_boxes 64-channel boxes; warps 1..3
@@ -373,6 +382,7 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
         }
         // The loads are in flight while the stage is awaited.
         if (b >= kStages) W.wait(bar(kBarKvEmpty + s), ((b / kStages) - 1) & 1);
+        if (*abort_flag) break;                  // the stage may still be in use
         uint8_t* rgen = sm + kOffTile + s * kTileBytes + row * 128;
 #pragma unroll
         for (int kk = 0; kk < 10; ++kk) {
@@ -398,11 +408,14 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
     const int n_boxes = a.n_boxes[r];
     const int w = warp - 1;                                   // 0..2
     const uint32_t tx_bytes = (uint32_t)(kBN / 4 / 3 * n_boxes * 512);
+    int issued = 0;
     for (int b = 0; b < nb; ++b) {
       const int s = b % kStages;
       if (b >= kStages) W.wait(bar(kBarKvEmpty + s), ((b / kStages) - 1) & 1);
       if (b >= 1 && b < kStages) W.wait(bar(kBarQStaged), 0);   // Q staging read
+      if (*abort_flag) break;                    // the stage may still be in use
       __syncwarp();
+      issued = b + 1;
       if (elect_one()) {
         const uint32_t full = bar(kBarKvFull + s);
         mbar_arrive_expect_tx(full, tx_bytes);
@@ -417,6 +430,15 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
       }
       __syncwarp();
     }
+    // Teardown: the gathers of the last block issued into each stage have
+    // landed (earlier ones were consumed before the stage was reissued).
+    // After an abort a stage's phase may lack another warp's share and wait
+    // out the limit; the copies themselves land within microseconds.
+    if (lane == 0) {
+      for (int b = issued - 1; b >= 0 && b >= issued - kStages; --b)
+        W.drain(bar(kBarKvFull + b % kStages), (b / kStages) & 1);
+    }
+    __syncwarp();
     }
   } else if (warp == 12) {
     // ---- signal warp: tell the peer when its partial scores were consumed --
@@ -704,7 +726,10 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
   // Each warpgroup's sends have read their stage; the peer's last X-free
   // arrivals land asynchronously: wait for the final phases of both X-free
   // barriers first.
-  if ((tid == 128 || tid == 256) && nb > 0) bulk_wait_read_all();
+  // (also after an abort: the peer's shared memory stays until the cluster
+  // barrier below, which this CTA passes only after its copies are complete)
+  if ((tid == 128 || tid == 256) && nb > 0) bulk_wait_all();
+  if (tid == 0 && a.q_tma) W.drain(bar(kBarQLoaded), 0);
   if (tid == 128 && nb > 0) {
     if (nb >= 2) W.wait(bar(kBarXFree + ((nb - 2) & 1)), ((nb - 2) >> 1) & 1);
     W.wait(bar(kBarXFree + ((nb - 1) & 1)), ((nb - 1) >> 1) & 1);
@@ -730,9 +755,7 @@ bool tc_supported(int h, int d_qk, int kv_format) {
          (kv_format == kBf16 || kv_format == kE4m3);
 }
 
-// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
-// (the library does not link libcuda directly).
-static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {

@@ -111,6 +111,7 @@ enum {
   kBarODone = kBarPEmpty + 2,
   kBarOFinal,                       // one phase: the unit's last PV is done
   kBarQReady,
+  kBarDrain,                        // teardown: both MMA warps' MMAs are done
   kNumBars
 };
 constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
@@ -194,7 +195,7 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
 
   auto bar = [&](int i) { return sb + kOffBar + 8u * (uint32_t)i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffAbort);
-  Waiter W{abort_flag, p.status};
+  Waiter W = make_waiter(abort_flag, p);
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -211,6 +212,7 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
     mbar_init(bar(kBarODone), 1);
     mbar_init(bar(kBarOFinal), 1);
     mbar_init(bar(kBarQReady), kSoftmax);
+    mbar_init(bar(kBarDrain), 2);
     *abort_flag = 0;
     fence_mbar_init_cluster();
   }
@@ -260,6 +262,7 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
         const uint32_t qb = sb + kOffQ;
         for (int j = 0; j < nb; ++j) {
           const int s = j & 1;
+          if (p.inject_stall && j == 0) continue;   // tests: block 0's scores never arrive
           W.wait(bar(kBarKvFull + s), (j >> 1) & 1);
           if (j >= 2) W.wait(bar(kBarSEmpty + s), ((j >> 1) - 1) & 1);
           __syncwarp();
@@ -327,6 +330,12 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
         }
       }
     }
+    // Every MMA this warp issued has completed (also after an abort) before
+    // the TMEM is freed and the tiles are left.
+    __syncwarp();
+    if (elect_one()) mma_commit(bar(kBarDrain));
+    __syncwarp();
+    W.drain(bar(kBarDrain), 0);
   } else if (warp <= 4) {
     // ---- loaders: a2 gather (+ a3 E4M3 conversion) -------------------------
     // Loader warp wl = warp - 1 owns tile rows [32 wl, 32 wl + 32): keys
@@ -407,6 +416,7 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
             sc[2] = kFmt == kE4m3Group ? __ldg(srow + 4) : kFmt == kDsMla ? 1.f : p.kpe_scale;
         }
         if (b >= kStages) W.wait(bar(kBarKvEmpty + s), ((b >> 1) - 1) & 1);
+        if (*abort_flag) break;                  // the stage may still be in use
         uint8_t* tile = sm + kOffTile + s * kStageBytes;
         // 16-byte unit cj (8 bf16 channels) of tile row `row`
         auto unit = [&](int row, uint32_t cj) -> uint4* {
@@ -451,10 +461,13 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
       // bf16: warp wl issues the 8 four-row groups of its 32 tile rows.
       const int n_boxes = ksteps > 16 ? 5 : 4;               // + one rope box
       const uint32_t tx_bytes = (uint32_t)(8 * n_boxes * 512);
+      int issued = 0;
       for (int b = 0; b < nb; ++b) {
         const int s = b & 1;
         if (b >= kStages) W.wait(bar(kBarKvEmpty + s), ((b >> 1) - 1) & 1);
+        if (*abort_flag) break;                  // the stage may still be in use
         __syncwarp();
+        issued = b + 1;
         if (elect_one()) {
           const uint32_t full = bar(kBarKvFull + s);
           mbar_arrive_expect_tx(full, tx_bytes);
@@ -470,6 +483,13 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
         }
         __syncwarp();
       }
+      // Teardown: the gathers of the last block issued into each stage have
+      // landed (see the heads-major kernel's producers).
+      if (lane == 0) {
+        for (int b = issued - 1; b >= 0 && b >= issued - kStages; --b)
+          W.drain(bar(kBarKvFull + (b & 1)), (b >> 1) & 1);
+      }
+      __syncwarp();
     }
   } else if (warp <= 8) {
     // ---- softmax warpgroup (thread <-> tile row <-> TMEM lane) ---------------

@@ -37,29 +37,46 @@ __device__ __forceinline__ bool named_bar_or(int id, int n, bool pred) {
   return out != 0u;
 }
 
-// Bounded waits.  A wait that runs out (or sees that another block already
-// gave up) records the timeout status, sets this block's abort flag, and from
-// then on every wait of the block returns at once, so the block still reaches
-// its teardown.  Results of an aborted launch are undefined; no access goes
-// out of bounds.
+// Bounded waits.  A wait that runs out (or sees that another block of the
+// same launch gave up) records the timeout status, bumps the device's abort
+// counter, sets this block's abort flag, and from then on every wait of the
+// block returns at once, so the block still reaches its teardown.  The
+// counter's value when the thread started is the launch's reference: a
+// timeout left over from an earlier launch (whose status word may still be
+// set) does not stop this one.  Results of an aborted launch are undefined;
+// no access goes out of bounds.
 struct Waiter {
-  volatile int* abort;
-  int* status;
+  volatile int* abort;   // this block's flag (shared memory)
+  int* status;           // device status word
+  int* ctr;              // device abort counter
+  int ctr0;              // its value when this thread started
+  uint64_t limit_ns;     // time limit of one wait
   __device__ __forceinline__ void fail() {
     if (!*abort) {
       *abort = 1;
+      atomicAdd(ctr, 1);
       atomicCAS(status, 0, kStatusTimeout);
     }
   }
   __device__ __forceinline__ void wait(uint32_t bar, uint32_t parity) {
     if (*abort) return;
-    if (!ptx::mbar_wait_bounded<false>(bar, parity, status, kStatusTimeout)) fail();
+    if (!ptx::mbar_wait_bounded<false>(bar, parity, limit_ns, ctr, ctr0)) fail();
   }
   __device__ __forceinline__ void wait_cluster(uint32_t bar, uint32_t parity) {
     if (*abort) return;
-    if (!ptx::mbar_wait_bounded<true>(bar, parity, status, kStatusTimeout)) fail();
+    if (!ptx::mbar_wait_bounded<true>(bar, parity, limit_ns, ctr, ctr0)) fail();
+  }
+  // Teardown: wait for asynchronous work this block started itself (TMA
+  // copies into its shared memory, MMAs reading it and writing its TMEM),
+  // also after an abort; only the time limit ends it.
+  __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
+    if (!ptx::mbar_wait_bounded<false>(bar, parity, limit_ns, nullptr, 0)) fail();
   }
 };
+__device__ __forceinline__ Waiter make_waiter(volatile int* abort_flag, const FwdParams& p) {
+  return Waiter{abort_flag, p.status, p.abort_ctr, *reinterpret_cast<volatile int*>(p.abort_ctr),
+                p.wait_limit_ns};
+}
 
 // Four E4M3 bytes -> four bf16 (two bf16x2 words), exactly: every E4M3 value
 // is a bf16 value.  The byte's exponent and mantissa fields are placed in the
@@ -281,6 +298,10 @@ static __device__ __noinline__ int lpt_unit(const FwdParams& p, int rank, int n_
   __syncthreads();
   return unit;
 }
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (the library does not link libcuda directly); nullptr if unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // A bf16 cache [num_slots, d_qk] as a 2-D tensor with 64-channel x 1-row
 // boxes and the 128-byte swizzle of the MMA operand tiles (TMA tile::gather4

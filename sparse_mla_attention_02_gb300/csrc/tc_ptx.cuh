@@ -76,13 +76,14 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // Bounded wait: returns false if the phase did not complete within
-// kWaitLimitNs, or as soon as *stop equals stop_value (another block gave
-// up), so that the caller records a timeout instead of hanging.
-constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;
+// limit_ns, or as soon as *stop differs from stop_value (stop = the device's
+// abort counter, stop_value = its value when the waiting thread started:
+// another block of the same launch gave up), so that the caller records a
+// timeout instead of hanging.  stop == nullptr: only the time limit.
 
 template <bool kCluster>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  const volatile int* stop,
+                                                  uint64_t limit_ns, const volatile int* stop,
                                                   int stop_value) {
   if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))
     return true;
@@ -91,8 +92,8 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))
       return true;
     if ((i & 255u) == 0u) {
-      if (*stop == stop_value) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+      if (stop && *stop != stop_value) return false;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
     }
   }
 }
@@ -150,6 +151,11 @@ __device__ __forceinline__ void bulk_commit_group() {
 // Wait until every committed bulk copy of this thread has read its source.
 __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until every committed bulk copy of this thread is complete (its
+// writes to the destination performed).
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // Hint: bring the cache line holding src into L2 without waiting for it.
@@ -292,6 +298,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
       "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
       "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
       : "memory");
 }
 

@@ -48,3 +48,31 @@ def dequant_rows_torch(w) -> torch.Tensor:
         return x * float(w.k_scale.cpu()[0])
     grp = torch.arange(w.d_qk) // 128
     return x * w.k_scale.cpu().to(torch.float64)[:, grp]
+
+
+# Out-of-bounds write check (compute-sanitizer is closed on this machine): output
+# and workspace buffers are carved out of a larger allocation whose first and
+# last GUARD bytes hold a sentinel; after the launch every sentinel byte must
+# be intact.  The buffer itself starts filled with the sentinel too, so a
+# value the kernel never wrote shows up as a mismatch against the oracle.
+GUARD = 4096
+SENTINEL = 0x5A
+
+
+class Guarded:
+    def __init__(self, shape, dtype, device="cuda"):
+        n = 1
+        for s in shape:
+            n *= int(s)
+        self.nbytes = n * torch.empty((), dtype=dtype).element_size()
+        self.buf = torch.full((GUARD + self.nbytes + GUARD,), SENTINEL,
+                              dtype=torch.uint8, device=device)
+        self.t = self.buf[GUARD:GUARD + self.nbytes].view(dtype).view(*shape)
+
+    def check(self, what=""):
+        lo = self.buf[:GUARD]
+        hi = self.buf[GUARD + self.nbytes:]
+        bad_lo = int((lo != SENTINEL).sum().item())
+        bad_hi = int((hi != SENTINEL).sum().item())
+        assert bad_lo == 0 and bad_hi == 0, \
+            f"{what}: {bad_lo} bytes written below and {bad_hi} above the buffer"

@@ -71,6 +71,42 @@ def test_bad_arguments_are_rejected_on_the_host(lib, kw, code):
     assert _fwd(lib, **kw) == code
 
 
+def _fwd_noalloc(lib, **kw):
+    a = dict(q=1 << 12, kv=1 << 12, kv_dtype=0, k_scale=None, idx=1 << 12,
+             valid=None, T=4, h=16, d_qk=576, d_v=512, topk=64, S=256,
+             scale=0.04, out=1 << 12, lse=None)
+    a.update(kw)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)
+    f = lib.smla_fwd_noalloc
+    VP, I, I64, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    f.argtypes = [VP, VP, I, VP, VP, VP, I, I, I, I, I, I64, F, VP, VP, VP]
+    f.restype = I
+    return lib.smla_fwd_noalloc(P(a["q"]), P(a["kv"]), a["kv_dtype"], P(a["k_scale"]),
+                                P(a["idx"]), P(a["valid"]), a["T"], a["h"], a["d_qk"],
+                                a["d_v"], a["topk"], a["S"], a["scale"], P(a["out"]),
+                                P(a["lse"]), None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=-1), 1), (dict(h=0), 1), (dict(topk=0), 1), (dict(S=0), 1),
+    (dict(h=200), 2), (dict(d_qk=128), 2), (dict(d_v=256), 2), (dict(kv_dtype=5), 2),
+    (dict(q=None), 1), (dict(out=(1 << 12) + 4), 1), (dict(valid=(1 << 12) + 2), 1),
+    # oversized shapes with a bad argument: the argument's code, not the
+    # scratch limit's
+    (dict(h=200, T=1 << 20, topk=1 << 16), 2), (dict(q=None, T=1 << 20, topk=1 << 16), 1),
+])
+def test_noalloc_rejects_what_smla_fwd_rejects(lib, kw, code):
+    """smla_fwd_noalloc runs smla_fwd's own checks before its scratch-size
+    check, so a call that smla_fwd would reject gets the same code."""
+    assert _fwd_noalloc(lib, **kw) == code
+    if "T" not in kw or kw["T"] >= 0:
+        assert _fwd(lib, **{k: v for k, v in kw.items()}) == code
+
+
+def test_stall_switch_argument_check(lib):
+    assert lib.smla_test_set_stall(1, -1) == 1
+
+
 def test_zero_tokens_is_ok_and_launches_nothing(lib):
     assert _fwd(lib, T=0, q=None, kv=None, idx=None, out=None) == 0
 

@@ -58,3 +58,34 @@ def test_job_throughput_is_weak_scaling():
     # 2 ranks, 10 units each per step, 3 steps, slowest rank 2 s -> 30 units/s
     assert bench.job_throughput(10, 2, 3, 2.0) == pytest.approx(30.0)
     assert bench.job_throughput(10, 1, 3, 1.0) == pytest.approx(30.0)
+
+
+def _bench(*argv):
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    return subprocess.run([sys.executable, os.path.join(root, "bench.py"), *argv],
+                          capture_output=True, text=True, timeout=600, env=env, cwd=root)
+
+
+def test_bench_spawns_its_ranks_when_run_without_a_launcher():
+    """bench.py --gpus 2 with no WORLD_SIZE starts two ranks itself (gloo for
+    the oracle arm here); rank 0 prints one line that counts both."""
+    import json
+    r = _bench("--impl", "reference", "--config", "tiny", "--gpus", "2", "--steps", "1",
+               "--warmup", "1", "--ref-tokens", "2")
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["n_gpus"] == 2 and d["impl"] == "reference"
+
+
+def test_bench_refuses_more_gpus_than_visible():
+    import torch
+    n = torch.cuda.device_count()
+    r = _bench("--gpus", str(n + 1), "--steps", "1", "--warmup", "3")
+    assert r.returncode != 0
+    assert not [l for l in r.stdout.splitlines() if l.startswith("{")]

@@ -18,7 +18,7 @@ import pytest
 import torch
 
 from sparse_mla_attention_02_gb300 import workloads as W
-from tests._helpers import oracle_fwd
+from tests._helpers import Guarded, oracle_fwd
 
 import oracle
 
@@ -29,11 +29,23 @@ TOL_LSE = 1e-3
 
 
 def gpu_fwd(smla, w, valid=True, indices=None, lse=True):
-    out, l = smla.smla_fwd(w.q, w.kv, w.kv_dtype, w.k_scale,
-                           w.indices if indices is None else indices,
-                           w.valid_len if valid else None, w.sm_scale,
-                           want_lse=lse, num_slots=w.num_slots)
+    """smla_fwd_ws with out, lse and the split workspace in guarded buffers
+    (sentinel bands before and after each, checked after the launch)."""
+    T, h = w.q.shape[0], w.q.shape[1]
+    go = Guarded((T, h, w.d_v), torch.bfloat16)
+    gl = Guarded((T, h), torch.float32) if lse else None
+    n = smla.smla_workspace_size(T, h, w.d_qk, w.indices.shape[1], w.kv_dtype)
+    gw = Guarded((n,), torch.uint8) if n > 0 else None
+    out, l = smla.smla_fwd_ws(w.q, w.kv, w.kv_dtype, w.k_scale,
+                              w.indices if indices is None else indices,
+                              w.valid_len if valid else None, w.sm_scale,
+                              None if gw is None else gw.t,
+                              out=go.t, lse=None if gl is None else gl.t,
+                              want_lse=lse, num_slots=w.num_slots)
     torch.cuda.synchronize()
+    for g, what in ((go, "out"), (gl, "lse"), (gw, "workspace")):
+        if g is not None:
+            g.check(f"{getattr(w, 'name', '')} {what}")
     return out, l
 
 

@@ -25,9 +25,12 @@ def plan(T, h, topk, kv=0, d_qk=576, sms=SMS):
 
 
 def family(h, kv):
-    if h <= 16:
-        return "tc_keys"
-    return "tc_heads" if kv in (0, 1) else "cuda_core"
+    """E4M3 caches with group scales (every layout, any h) and per-tensor
+    E4M3 with h <= 16: the E4M3-operand keys-major kernel; bf16 with h <= 16:
+    the bf16 keys-major kernel; the rest: the heads-major kernel."""
+    if kv in (2, 3, 4) or (kv == 1 and h <= 16):
+        return "tc_keys_fp8"
+    return "tc_keys" if h <= 16 else "tc_heads"
 
 
 def test_benchmark_workloads_run_unsplit():
@@ -35,12 +38,19 @@ def test_benchmark_workloads_run_unsplit():
     assert plan(8192, 128, 2048) == {"kernel": "tc_heads", "splits": 1, "workspace_bytes": 0}
     assert plan(64, 128, 2048) == {"kernel": "tc_heads", "splits": 1, "workspace_bytes": 0}
     assert plan(128, 64, 2048, kv=1, d_qk=512)["splits"] == 1
-    assert plan(16384, 16, 2048, kv=2) == {"kernel": "tc_keys", "splits": 1, "workspace_bytes": 0}
+    assert plan(16384, 16, 2048, kv=2) == {"kernel": "tc_keys_fp8", "splits": 1,
+                                           "workspace_bytes": 0}
+    assert plan(128, 128, 2048, kv=3)["splits"] == 1
 
 
 def test_few_tokens_split_to_fill_the_gpu():
     p = plan(2, 16, 2048, kv=2)                 # one CTA per unit, 152 SMs
+    assert p["kernel"] == "tc_keys_fp8" and p["splits"] == 16
+    p = plan(2, 16, 2048, kv=0)
     assert p["kernel"] == "tc_keys" and p["splits"] == 16
+    p = plan(2, 64, 2048, kv=3)                 # 4 head groups per token
+    assert p["kernel"] == "tc_keys_fp8" and p["splits"] == 16
+    assert plan(8, 128, 2048, kv=2)["splits"] == 2   # 8 tokens x 8 head groups
     p = plan(4, 128, 2048)                      # a cluster of two SMs per unit
     assert p["kernel"] == "tc_heads" and 2 <= p["splits"] <= 16
     assert plan(1, 128, 64)["splits"] == 1      # 64 positions: nothing to split
@@ -78,12 +88,13 @@ def test_plan_invariants_over_random_shapes():
         assert sp >= 1
         assert ws == (4 * sp * T * h * 513 if sp > 1 else 0), (T, h, topk, sp, ws)
         if p["kernel"] != "cuda_core":
-            rng_len = KEYS_RANGE if p["kernel"] == "tc_keys" else HEADS_RANGE
+            rng_len = HEADS_RANGE if p["kernel"] == "tc_heads" else KEYS_RANGE
             need = math.ceil(topk / rng_len)
             assert sp >= need, (T, h, topk, sp)
             assert sp <= max(16, need), (T, h, topk, sp)
-            places = sms if p["kernel"] == "tc_keys" else max(sms // 2, 1)
-            if 2 * T >= places:                 # the tokens fill the GPU
+            places = max(sms // 2, 1) if p["kernel"] == "tc_heads" else sms
+            per_token = math.ceil(h / 16) if p["kernel"] == "tc_keys_fp8" else 1
+            if 2 * T * per_token >= places:     # the tokens fill the GPU
                 assert sp == need, (T, h, topk, sms, sp)
         # more tokens never split more
         assert plan(2 * T, h, topk, kv=kv, d_qk=d_qk, sms=sms)["splits"] <= sp

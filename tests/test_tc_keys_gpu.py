@@ -23,13 +23,17 @@ from tests.test_parity_gpu import check, compare, gpu_fwd
 pytestmark = pytest.mark.gpu
 
 
-def test_dispatch_uses_keys_kernel_up_to_16_heads(cuda_lib):
+def test_dispatch_uses_keys_kernels_up_to_16_heads(cuda_lib):
     for kv in (0, 1, 2):
         for h in (1, 7, 16):
             for d in (512, 576):
                 info = cuda_lib.smla_plan_info(512, h, d, 2048, kv)
-                assert info["kernel"] == "tc_keys", (kv, h, d, info)
+                want = "tc_keys" if kv == 0 else "tc_keys_fp8"
+                assert info["kernel"] == want, (kv, h, d, info)
     assert cuda_lib.smla_plan_info(512, 17, 576, 2048, 0)["kernel"] == "tc_heads"
+    assert cuda_lib.smla_plan_info(512, 17, 576, 2048, 1)["kernel"] == "tc_heads"
+    for kv in (2, 3, 4):
+        assert cuda_lib.smla_plan_info(512, 128, 576, 2048, kv)["kernel"] == "tc_keys_fp8"
     assert cuda_lib.smla_plan_info(512, 16, 576, 4096, 2)["splits"] >= 2
 
 
