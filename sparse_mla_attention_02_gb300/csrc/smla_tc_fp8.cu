@@ -35,7 +35,8 @@
 // prefix with -1 past it; vLLM API docs flashmla_sparse,
 // _forward_fp8_kv_mixed_batch: empty rows give (O = 0, LSE = -inf)):
 //   a1 work setup: v = min(valid_len[t], topk); range [k0, k1) of the split
-//   a2 gather: slot ids -> TMA tile::gather4 of raw rows (masked: zero fill)
+//   a2 gather: slot ids -> raw rows: TMA tile::gather4 for the ckv chunks,
+//      cp.async for the rope (masked rows: zero fill)
 //   a3 scales: per-tensor scale on the score scale and the output; group
 //      scales on the group accumulators (QK) and inside P' (PV)
 //   a4 QK^T, a5 masked online softmax, a6 PV, a7 O / l and LSE = m + ln l
@@ -79,6 +80,10 @@ constexpr int kThreads = 448;
 constexpr int kProducers = 128;            // warps 1..4
 constexpr int kSoftmax = 256;              // warps 5..12
 constexpr int kMaxBlocks = 16;             // ranges up to 2048 positions
+// ckv chunks gathered by TMA (the rest and the rope by cp.async).  Mixed FP8
+// batch: 4 -> 3.06 ms, 3 -> 3.27, 2 -> 3.62, 0 -> 3.81; the rope box by TMA
+// as well (128 bytes of which 64 are real for E4M3 rows) 3.26 ms.
+constexpr int kTmaChunks = 4;
 constexpr float kT = 4.f;                  // lazy max threshold (log2 units)
 constexpr float kPShift = 16.f;            // 2^(8 - kT): P' <= 2^8
 
@@ -238,7 +243,9 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(kBarKvFull + s), 4);          // one expect_tx per producer warp
+      // one expect_tx per producer warp (TMA part) + one cp.async arrival per
+      // producer thread
+      mbar_init(bar(kBarKvFull + s), (kTmaChunks > 0 ? 4 : 0) + kProducers);
       mbar_init(bar(kBarKvEmpty + s), 1);
       mbar_init(bar(kBarSFull + s), 1);
       mbar_init(bar(kBarSEmpty + s), kSoftmax);
@@ -374,13 +381,20 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
     __syncwarp();
     W.drain(bar(kBarDrain), 0);
   } else if (warp <= 4) {
-    // ---- producers: a2 gather (TMA tile::gather4 of raw rows) ---------------
-    // Warp wl issues tile rows [32 wl, 32 wl + 32): 8 groups of 4 rows x the
-    // row's 128-byte boxes.  A masked position (slot id -1) reads the
-    // out-of-bounds fill, a zero row.
+    // ---- producers: a2 gather of raw rows -------------------------------------
+    // Warp wl fills tile rows [32 wl, 32 wl + 32).  The first kTmaChunks
+    // 128-byte ckv chunks of each row come by TMA tile::gather4 (8 groups of
+    // 4 rows per warp; a masked position, slot id -1, reads the out-of-bounds
+    // zero fill); the other ckv chunks and the rope by 16-byte cp.async from
+    // the warp's lanes (consecutive lanes on consecutive pieces of a row;
+    // masked rows are zero-filled without a read), which run beside the TMA
+    // engine.  The rope piece count: 4 (64 E4M3 bytes) or 8 (64 bf16 values).
     const int wl = warp - 1;
-    const int n_boxes = rope ? 5 : 4;
-    const uint32_t tx_bytes = (uint32_t)(8 * n_boxes * 512);
+    constexpr int kRopePieces = kBf16Rope ? 8 : 4;
+    const int n_cp = (4 - kTmaChunks) * 8 + (rope ? kRopePieces : 0);   // pieces a row
+    const int row_bytes = kFmt == kDsMla ? kDsMlaRowBytes : p.d_qk;
+    const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
+    const uint32_t tx_bytes = (uint32_t)(8 * kTmaChunks * 512);
     int issued = 0;
     for (int b = 0; b < nb; ++b) {
       const int s = b & 1;
@@ -388,23 +402,45 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
       if (*abort_flag) break;                    // the stage may still be in use
       __syncwarp();
       issued = b + 1;
-      if (elect_one()) {
-        const uint32_t full = bar(kBarKvFull + s);
+      const uint32_t full = bar(kBarKvFull + s);
+      const uint32_t tile = sb + kOffTile + s * kStageBytes;
+      const int* bs = slots + b * kBK + 32 * wl;
+      if (kTmaChunks > 0 && elect_one()) {
         mbar_arrive_expect_tx(full, tx_bytes);
-        const uint32_t tile = sb + kOffTile + s * kStageBytes;
-        const int* bs = slots + b * kBK + 32 * wl;
         for (int g = 0; g < 8; ++g) {
           const int y0 = bs[4 * g], y1 = bs[4 * g + 1], y2 = bs[4 * g + 2], y3 = bs[4 * g + 3];
-          for (int c = 0; c < n_boxes; ++c)
-            tma_gather4(tile + c * kChunkBytes + (32 * wl + 4 * g) * 128, &a.kv_map,
-                        c < 4 ? 128 * c : a.rope_x, y0, y1, y2, y3, full);
+          for (int c = 0; c < kTmaChunks; ++c)
+            tma_gather4(tile + c * kChunkBytes + (32 * wl + 4 * g) * 128, &a.kv_map, 128 * c, y0,
+                        y1, y2, y3, full);
         }
       }
       __syncwarp();
+      for (int e = lane; e < 32 * n_cp; e += 32) {
+        const int r = e / n_cp, k = e - r * n_cp;      // row of the warp, piece of the row
+        const int id = bs[r];
+        const int row = 32 * wl + r;
+        int c, u, src_off;
+        if (k < (4 - kTmaChunks) * 8) {
+          c = kTmaChunks + (k >> 3);
+          u = k & 7;
+          src_off = 128 * c + 16 * u;
+        } else {
+          c = 4;
+          u = k - (4 - kTmaChunks) * 8;
+          src_off = a.rope_x + 16 * u;
+        }
+        const uint32_t dst =
+            tile + (uint32_t)(c * kChunkBytes + row * 128) + ((uint32_t)(u ^ (row & 7)) << 4);
+        const uint8_t* src = kv8 + (size_t)(id < 0 ? 0 : id) * row_bytes + src_off;
+        cp_async16(dst, src, id < 0 ? 0u : 16u);
+      }
+      cp_async_arrive_noinc(full);
     }
-    // Teardown: the gathers of the last block issued into each stage have
-    // landed (earlier ones were consumed before the stage was reissued).
-    if (lane == 0) {
+    // Teardown: this thread's copies have landed; the gathers of the last
+    // block issued into each stage too (earlier ones were consumed before the
+    // stage was reissued).
+    cp_async_wait_all();
+    if (kTmaChunks > 0 && lane == 0) {
       for (int b = issued - 1; b >= 0 && b >= issued - kStages; --b)
         W.drain(bar(kBarKvFull + (b & 1)), (b >> 1) & 1);
     }

@@ -125,6 +125,22 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int 
       : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only, .cg); src_bytes = 0
+// writes 16 zero bytes without reading global memory.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+// Arrive on `bar` once every cp.async this thread issued before has landed
+// (the arrival is one of the barrier's expected arrivals: .noinc).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // TMA tiled 2-D load of one box at coordinates (x, y), counted on `bar`.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y,
                                             uint32_t bar) {
