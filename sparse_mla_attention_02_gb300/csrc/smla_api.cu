@@ -186,6 +186,7 @@ smla_status run_fwd(const void* q, const void* kv, int kv_dtype,
   p.d_qk = d_qk;
   p.d_v = d_v;
   p.topk = topk;
+  p.num_sms = dev->num_sms;
   p.splits = plan.splits;
   p.split_len = plan.split_len;
   p.sm_scale = sm_scale;

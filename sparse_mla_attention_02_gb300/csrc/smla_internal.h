@@ -41,6 +41,7 @@ struct FwdParams {
   int64_t num_slots;
   int kv_format;
   int T, h, d_qk, d_v, topk;
+  int num_sms;            // SMs of the device (persistent launches)
   int splits;             // top-k position ranges per (token, head group)
   int split_len;          // positions per range
   int lpt;                // take the units longest first (lpt_unit): more

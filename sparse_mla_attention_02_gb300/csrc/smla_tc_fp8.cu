@@ -80,10 +80,6 @@ constexpr int kThreads = 448;
 constexpr int kProducers = 128;            // warps 1..4
 constexpr int kSoftmax = 256;              // warps 5..12
 constexpr int kMaxBlocks = 16;             // ranges up to 2048 positions
-// ckv chunks gathered by TMA (the rest and the rope by cp.async).  Mixed FP8
-// batch: 4 -> 3.06 ms, 3 -> 3.27, 2 -> 3.62, 0 -> 3.81; the rope box by TMA
-// as well (128 bytes of which 64 are real for E4M3 rows) 3.26 ms.
-constexpr int kTmaChunks = 4;
 constexpr float kT = 4.f;                  // lazy max threshold (log2 units)
 constexpr float kPShift = 16.f;            // 2^(8 - kT): P' <= 2^8
 
@@ -94,26 +90,31 @@ constexpr uint32_t kSBuf = 5 * kNq;
 constexpr uint32_t kTmemCols = 512;
 static_assert(kColS + 2 * kSBuf <= kTmemCols, "TMEM budget");
 
-// Shared-memory layout (offsets from a 1024-byte aligned base).
+// Shared-memory layout (offsets from a 1024-byte aligned base).  The tile
+// stages carry, beside the rows, each block's valid-bit words and (group
+// formats) its keys' scales, written by the producers with the gathers.
+constexpr int kScaleRow = 5;                                       // floats per key
 constexpr uint32_t kOffTile = 0;
 constexpr uint32_t kOffQ = kOffTile + kStages * kStageBytes;       // Q' chunks
-constexpr uint32_t kOffP = kOffQ + kMaxChunks * kQChunkBytes;      // P' [2]
-constexpr uint32_t kOffSlot = kOffP + 2 * kPBytes;                 // [blocks*128] i32
-constexpr uint32_t kOffMask = kOffSlot + kMaxBlocks * kBK * 4;     // [blocks][4] u32
-constexpr uint32_t kOffRed = kOffMask + kMaxBlocks * 16;           // [2 wg][4 warps][8] f32
+constexpr uint32_t kOffP = kOffQ + kMaxChunks * kQChunkBytes;      // P' (one buffer)
+constexpr uint32_t kOffSlot = kOffP + kPBytes;                     // [blocks*128] i32
+constexpr uint32_t kOffSc = kOffSlot + kMaxBlocks * kBK * 4;       // [2][128][5] f32
+constexpr uint32_t kOffMask = kOffSc + kStages * kBK * kScaleRow * 4;  // [2][4] u32
+constexpr uint32_t kOffRed = kOffMask + kStages * 16;              // [2 wg][4 warps][8] f32
 constexpr uint32_t kOffRedSc = kOffRed + 2 * 4 * 8 * 4;            // [2 wg][4 warps][4] f32
 constexpr uint32_t kOffQf = kOffRedSc + 2 * 4 * 4 * 4;             // [16] f32: 2^-a per head
-constexpr uint32_t kOffBar = kOffQf + kHeads * 4;
+constexpr uint32_t kOffOst = kOffQf + kHeads * 4;                  // [16 heads][512] bf16
+constexpr uint32_t kOffBar = kOffOst + kHeads * 512 * 2;
 enum {
-  kBarKvFull = 0,                   // [2]
+  kBarKvFull = 0,                   // [2] the tile, masks and scales of a block
   kBarKvEmpty = kBarKvFull + 2,     // [2]
   kBarSFull = kBarKvEmpty + 2,      // [2]
   kBarSEmpty = kBarSFull + 2,       // [2]
-  kBarPFull = kBarSEmpty + 2,       // [2]
-  kBarPEmpty = kBarPFull + 2,       // [2]
-  kBarODone = kBarPEmpty + 2,
-  kBarOFinal,                       // one phase: the unit's last PV is done
-  kBarQReady,
+  kBarPFull = kBarSEmpty + 2,
+  kBarPEmpty,
+  kBarODone,
+  kBarOFinal,                       // one phase per unit: its last PV is done
+  kBarQReady,                       // one phase per unit: Q' written
   kBarDrain,                        // teardown: both MMA warps' MMAs are done
   kNumBars
 };
@@ -122,12 +123,13 @@ constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
 constexpr uint32_t kSmemBytes = kOffAbort + 4 + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzled operands need 1024-B alignment");
-static_assert(kOffRed % 16 == 0 && kOffBar % 8 == 0, "alignment");
+static_assert(kOffRed % 16 == 0 && kOffOst % 16 == 0 && kOffBar % 8 == 0, "alignment");
 
 struct Fp8Args {
   CUtensorMap kv_map;  // the cache as bytes [num_slots, row bytes], 128-byte boxes
   FwdParams p;
-  int n_hg;            // head groups of 16 (CTAs per token and range)
+  int n_hg;            // head groups of 16 (units per token and range)
+  int n_units;         // T * splits * n_hg; CTA c runs units c, c + grid, ...
   int rope_x;          // byte offset of the rope box in a row (576-channel rows)
   int G;               // scales per slot (E4M3 group format)
   float scale_log2;    // sm_scale * log2(e)
@@ -208,6 +210,39 @@ __device__ __forceinline__ float pow2_at_most_inv(float x) {
   return pow2i(max(-126, min(126, -e)));
 }
 
+// The unit u of the launch: (token, range) * n_hg + head group (the head
+// groups of a token select the same rows and run side by side), its valid
+// range [k0, k1) and its blocks.
+struct UnitInfo {
+  int t, split, h0, k0, k1, nb;
+};
+__device__ __forceinline__ UnitInfo unit_info(const Fp8Args& a, int u) {
+  const FwdParams& p = a.p;
+  UnitInfo ui;
+  const int hg = u % a.n_hg;
+  const int ts = u / a.n_hg;
+  ui.split = ts % p.splits;
+  ui.t = ts / p.splits;
+  ui.h0 = kHeads * hg;
+  int v = p.topk;
+  if (p.valid_len) v = min(max(__ldg(p.valid_len + ui.t), 0), p.topk);
+  ui.k0 = ui.split * p.split_len;
+  ui.k1 = min(ui.k0 + p.split_len, v);
+  // The host plan keeps every range within kMaxBlocks blocks.
+  ui.nb = ui.k1 > ui.k0 ? min((ui.k1 - ui.k0 + kBK - 1) / kBK, kMaxBlocks) : 0;
+  return ui;
+}
+
+// Persistent: each CTA runs units blockIdx.x, blockIdx.x + gridDim.x, ...
+// in that order.  Every role walks the same sequence of units and skips the
+// empty ones (no block), so that the CTA's running block count g (and the
+// running count of non-empty units) name the same barrier phases in every
+// role: block g uses stage g & 1 with phase (g >> 1) & 1, and the per-unit
+// barriers (Q ready, last PV done) have one phase per non-empty unit.  The
+// pipeline runs across unit boundaries: the producers load the next unit's
+// slot ids right after issuing the current unit's last gathers, and the
+// softmax warps write the next unit's Q' once the current unit's QK MMAs
+// are done (after its last scores were read), before its epilogue.
 template <int kFmt>
 __global__ void __launch_bounds__(kThreads, 1)
 smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
@@ -219,23 +254,8 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
   const uint32_t sb = (raw + 1023u) & ~1023u;           // shared address base
   uint8_t* sm = smem_raw + (sb - raw);                  // generic pointer base
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  // ---- a1: work unit ------------------------------------------------------
-  // unit = (token, range) * n_hg + head group: the head groups of a token
-  // select the same rows and run side by side.
-  int unit = (int)blockIdx.x;
-  const int hg = unit % a.n_hg;
-  unit /= a.n_hg;
-  const int split = unit % p.splits;
-  const int t = unit / p.splits;
-  const int h0 = kHeads * hg;                           // first head of the CTA
-  int v = p.topk;
-  if (p.valid_len) v = min(max(__ldg(p.valid_len + t), 0), p.topk);
-  const int k0 = split * p.split_len;
-  const int k1 = min(k0 + p.split_len, v);
-  // The host plan keeps every range within kMaxBlocks blocks.
-  const int nb = k1 > k0 ? min((k1 - k0 + kBK - 1) / kBK, kMaxBlocks) : 0;
   const bool rope = p.d_qk == 576;
+  const int u_step = (int)gridDim.x;
 
   auto bar = [&](int i) { return sb + kOffBar + 8u * (uint32_t)i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffAbort);
@@ -243,15 +263,15 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      // one expect_tx per producer warp (TMA part) + one cp.async arrival per
-      // producer thread
-      mbar_init(bar(kBarKvFull + s), (kTmaChunks > 0 ? 4 : 0) + kProducers);
+      // one expect_tx per producer warp (TMA), one cp.async arrival and one
+      // plain arrival (masks and scales stored) per producer thread
+      mbar_init(bar(kBarKvFull + s), 4 + 2 * kProducers);
       mbar_init(bar(kBarKvEmpty + s), 1);
       mbar_init(bar(kBarSFull + s), 1);
       mbar_init(bar(kBarSEmpty + s), kSoftmax);
-      mbar_init(bar(kBarPFull + s), kSoftmax);
-      mbar_init(bar(kBarPEmpty + s), 1);
     }
+    mbar_init(bar(kBarPFull), kSoftmax);
+    mbar_init(bar(kBarPEmpty), 1);
     mbar_init(bar(kBarODone), 1);
     mbar_init(bar(kBarOFinal), 1);
     mbar_init(bar(kBarQReady), kSoftmax);
@@ -269,110 +289,63 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + kOffTmemSlot);
 
-  // a1/a2 setup: the producers read the unit's index range once into shared
-  // memory (masked: past k1, < 0, >= num_slots), then one valid-bit word per
-  // 32 keys of each block.
-  int* slots = reinterpret_cast<int*>(sm + kOffSlot);
-  uint32_t* masks = reinterpret_cast<uint32_t*>(sm + kOffMask);
-  if (warp >= 1 && warp <= 4) {
-    const int pt = tid - 32;
-    if (load_unit_slots(p, t, k0, k1, nb * kBK, slots, pt, kProducers))
-      atomicCAS(p.status, 0, kStatusBadIndex);
-    named_bar_sync(1, kProducers);
-    const int wl = warp - 1;
-    for (int b = 0; b < nb; ++b) {
-      const uint32_t m = __ballot_sync(0xffffffffu, slots[b * kBK + 32 * wl + lane] >= 0);
-      if (lane == 0) masks[b * 4 + wl] = m;
-    }
-  }
-  __syncthreads();
-
-  if (warp == 0 || warp == 13) {
-    // ---- MMA issuers: warp 0 issues QK, warp 13 issues PV ----------------
-    if (nb > 0) {
-      if (warp == 0) {
-        const uint32_t id_qk = idesc_e4m3(128, kNq, false, false);
-        const uint32_t id_rope = idesc_bf16(128, kHeads, false, false);
-        W.wait(bar(kBarQReady), 0);
+  if (warp == 0) {
+    // ---- QK issuer ------------------------------------------------------
+    const uint32_t id_qk = idesc_e4m3(128, kNq, false, false);
+    const uint32_t id_rope = idesc_bf16(128, kHeads, false, false);
+    const uint32_t qb = sb + kOffQ;
+    int g = 0, ku = 0;
+    for (int u = blockIdx.x; u < a.n_units; u += u_step) {
+      const UnitInfo ui = unit_info(a, u);
+      if (ui.nb == 0) continue;
+      W.wait(bar(kBarQReady), ku & 1);
+      tc_fence_after();
+      for (int j = 0; j < ui.nb; ++j, ++g) {
+        const int s = g & 1;
+        if (p.inject_stall && j == 0) continue;   // tests: block 0's scores never arrive
+        W.wait(bar(kBarKvFull + s), (g >> 1) & 1);
+        if (g >= 2) W.wait(bar(kBarSEmpty + s), ((g >> 1) - 1) & 1);
+        __syncwarp();
         tc_fence_after();
-        const uint32_t qb = sb + kOffQ;
-        for (int j = 0; j < nb; ++j) {
-          const int s = j & 1;
-          if (p.inject_stall && j == 0) continue;   // tests: block 0's scores never arrive
-          W.wait(bar(kBarKvFull + s), (j >> 1) & 1);
-          if (j >= 2) W.wait(bar(kBarSEmpty + s), ((j >> 1) - 1) & 1);
-          __syncwarp();
-          tc_fence_after();
-          const uint32_t tile = sb + kOffTile + s * kStageBytes;
-          const uint32_t dS = tmem + kColS + kSBuf * s;
-          if (elect_one()) {
-            // A = 128 key rows, K-major; B = Q' rows, K-major; a step is 32
-            // E4M3 channels (32 bytes of a 128-byte swizzled row).  Group c
-            // of the ckv accumulates into columns [32 c, 32 c + 32).
-            const uint64_t a0 = sdesc(tile, 16, 1024, kLayoutSw128);
-            const uint64_t b0 = sdesc(qb, 16, 1024, kLayoutSw128);
+        const uint32_t tile = sb + kOffTile + s * kStageBytes;
+        const uint32_t dS = tmem + kColS + kSBuf * s;
+        if (elect_one()) {
+          fence_proxy_async_smem();
+          // A = 128 key rows, K-major; B = Q' rows, K-major; a step is 32
+          // E4M3 channels (32 bytes of a 128-byte swizzled row).  Group c of
+          // the ckv accumulates into columns [32 c, 32 c + 32).
+          const uint64_t a0 = sdesc(tile, 16, 1024, kLayoutSw128);
+          const uint64_t b0 = sdesc(qb, 16, 1024, kLayoutSw128);
 #pragma unroll
-            for (int ks = 0; ks < 16; ++ks) {
-              const uint32_t oa = (uint32_t)((ks >> 2) * kChunkBytes + (ks & 3) * 32);
-              const uint32_t ob = (uint32_t)((ks >> 2) * kQChunkBytes + (ks & 3) * 32);
-              const uint32_t acc = kGroup ? (uint32_t)(ks >> 2) * kNq : 0u;
-              const bool first = kGroup ? (ks & 3) == 0 : ks == 0;
-              mma_f8(dS + acc, a0 + (oa >> 4), b0 + (ob >> 4), id_qk, first ? 0u : 1u);
-            }
-            if (rope) {
-              const uint32_t oa = (uint32_t)(4 * kChunkBytes), ob = (uint32_t)(4 * kQChunkBytes);
-              if (kBf16Rope) {
-                // 64 bf16 rope channels (one 128-byte chunk) x 16 bf16 Q rows
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                  mma_ss(dS + 4 * kNq, a0 + ((oa + 32 * ks) >> 4), b0 + ((ob + 32 * ks) >> 4),
-                         id_rope, ks > 0 ? 1u : 0u);
-              } else {
-                // 64 E4M3 rope channels: two steps (the chunk's other 64
-                // bytes are the zero fill past the row)
-#pragma unroll
-                for (int ks = 0; ks < 2; ++ks)
-                  mma_f8(dS + (kGroup ? 4 * kNq : 0u), a0 + ((oa + 32 * ks) >> 4),
-                         b0 + ((ob + 32 * ks) >> 4), id_qk, (kGroup && ks == 0) ? 0u : 1u);
-              }
-            }
-            mma_commit(bar(kBarSFull + s));
+          for (int ks = 0; ks < 16; ++ks) {
+            const uint32_t oa = (uint32_t)((ks >> 2) * kChunkBytes + (ks & 3) * 32);
+            const uint32_t ob = (uint32_t)((ks >> 2) * kQChunkBytes + (ks & 3) * 32);
+            const uint32_t acc = kGroup ? (uint32_t)(ks >> 2) * kNq : 0u;
+            const bool first = kGroup ? (ks & 3) == 0 : ks == 0;
+            mma_f8(dS + acc, a0 + (oa >> 4), b0 + (ob >> 4), id_qk, first ? 0u : 1u);
           }
-          __syncwarp();
-        }
-      } else {
-        const uint32_t id_pv = idesc_e4m3(128, kNq, true, true);
-        for (int j = 0; j < nb; ++j) {
-          const int s = j & 1;
-          W.wait(bar(kBarPFull + s), (j >> 1) & 1);
-          __syncwarp();
-          tc_fence_after();
-          const uint32_t tile = sb + kOffTile + s * kStageBytes;
-          const uint32_t pb = sb + kOffP + s * kPBytes;
-          if (elect_one()) {
-            // A = V^T of channel block c: chunk c (128 channels) x 32 keys,
-            // MN-major; B = P'^T: 32 keys x 32, MN-major (group scales:
-            // group c's 32 bytes of each key's row).
+          if (rope) {
+            const uint32_t oa = (uint32_t)(4 * kChunkBytes), ob = (uint32_t)(4 * kQChunkBytes);
+            if (kBf16Rope) {
+              // 64 bf16 rope channels (one 128-byte chunk) x 16 bf16 Q rows
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+              for (int ks = 0; ks < 4; ++ks)
+                mma_ss(dS + 4 * kNq, a0 + ((oa + 32 * ks) >> 4), b0 + ((ob + 32 * ks) >> 4),
+                       id_rope, ks > 0 ? 1u : 0u);
+            } else {
+              // 64 E4M3 rope channels: two steps (the rest of the chunk is
+              // not read)
 #pragma unroll
-              for (int ks = 0; ks < kBK / 32; ++ks) {
-                const uint64_t ad =
-                    sdesc(tile + c * kChunkBytes + ks * 4096, kChunkBytes, 1024, kLayoutSw128);
-                const uint64_t bd = sdesc(pb + ks * 4096 + (kGroup ? 32 * c : 0), kPBytes, 1024,
-                                          kLayoutSw128);
-                mma_f8(tmem + kColO + 32u * (uint32_t)c, ad, bd, id_pv,
-                       (j > 0 || ks > 0) ? 1u : 0u);
-              }
+              for (int ks = 0; ks < 2; ++ks)
+                mma_f8(dS + (kGroup ? 4 * kNq : 0u), a0 + ((oa + 32 * ks) >> 4),
+                       b0 + ((ob + 32 * ks) >> 4), id_qk, (kGroup && ks == 0) ? 0u : 1u);
             }
-            mma_commit(bar(kBarODone));
-            mma_commit(bar(kBarPEmpty + s));
-            mma_commit(bar(kBarKvEmpty + s));
-            if (j == nb - 1) mma_commit(bar(kBarOFinal));
           }
-          __syncwarp();
+          mma_commit(bar(kBarSFull + s));
         }
+        __syncwarp();
       }
+      ++ku;
     }
     // Every MMA this warp issued has completed (also after an abort) before
     // the TMEM is freed and the tiles are left.
@@ -380,67 +353,147 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
     if (elect_one()) mma_commit(bar(kBarDrain));
     __syncwarp();
     W.drain(bar(kBarDrain), 0);
+  } else if (warp == 13) {
+    // ---- PV issuer ------------------------------------------------------
+    const uint32_t id_pv = idesc_e4m3(128, kNq, true, true);
+    const uint32_t pb = sb + kOffP;
+    int g = 0;
+    for (int u = blockIdx.x; u < a.n_units; u += u_step) {
+      const UnitInfo ui = unit_info(a, u);
+      for (int j = 0; j < ui.nb; ++j, ++g) {
+        const int s = g & 1;
+        W.wait(bar(kBarPFull), g & 1);
+        __syncwarp();
+        tc_fence_after();
+        const uint32_t tile = sb + kOffTile + s * kStageBytes;
+        if (elect_one()) {
+          fence_proxy_async_smem();
+          // A = V^T of channel block c: chunk c (128 channels) x 32 keys,
+          // MN-major; B = P'^T: 32 keys x 32, MN-major (group scales: group
+          // c's 32 bytes of each key's row).  The unit's first block
+          // overwrites O (the softmax warps read the previous unit's O before
+          // they handed over this P').
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+#pragma unroll
+            for (int ks = 0; ks < kBK / 32; ++ks) {
+              const uint64_t ad =
+                  sdesc(tile + c * kChunkBytes + ks * 4096, kChunkBytes, 1024, kLayoutSw128);
+              const uint64_t bd =
+                  sdesc(pb + ks * 4096 + (kGroup ? 32 * c : 0), kPBytes, 1024, kLayoutSw128);
+              mma_f8(tmem + kColO + 32u * (uint32_t)c, ad, bd, id_pv,
+                     (j > 0 || ks > 0) ? 1u : 0u);
+            }
+          }
+          mma_commit(bar(kBarODone));
+          mma_commit(bar(kBarPEmpty));
+          mma_commit(bar(kBarKvEmpty + s));
+          if (j == ui.nb - 1) mma_commit(bar(kBarOFinal));
+        }
+        __syncwarp();
+      }
+    }
+    __syncwarp();
+    if (elect_one()) mma_commit(bar(kBarDrain));
+    __syncwarp();
+    W.drain(bar(kBarDrain), 0);
   } else if (warp <= 4) {
-    // ---- producers: a2 gather of raw rows -------------------------------------
-    // Warp wl fills tile rows [32 wl, 32 wl + 32).  The first kTmaChunks
-    // 128-byte ckv chunks of each row come by TMA tile::gather4 (8 groups of
-    // 4 rows per warp; a masked position, slot id -1, reads the out-of-bounds
-    // zero fill); the other ckv chunks and the rope by 16-byte cp.async from
-    // the warp's lanes (consecutive lanes on consecutive pieces of a row;
-    // masked rows are zero-filled without a read), which run beside the TMA
-    // engine.  The rope piece count: 4 (64 E4M3 bytes) or 8 (64 bf16 values).
+    // ---- producers: slot ids, then a2 gather of raw rows ------------------
+    // Per unit the four warps read its index range into shared memory
+    // (masked: past k1, < 0, >= num_slots); only they read it.  Per block,
+    // warp wl fills tile rows [32 wl, 32 wl + 32): the four 128-byte ckv
+    // chunks by TMA tile::gather4 (8 groups of 4 rows; a masked position,
+    // slot id -1, reads the out-of-bounds zero fill), the rope by 16-byte
+    // cp.async (zero-filled for masked rows), and the row's valid bit and
+    // group scales into the stage.  (Measured on the mixed FP8 batch: the
+    // four ckv chunks by TMA and the 64-byte rope by cp.async 3.06 ms; the
+    // rope as a 128-byte TMA box too, 64 bytes of it fill, 3.26 ms; moving
+    // ckv chunks to cp.async 3.27 ms (one), 3.62 (two), 3.81 (all four).)
     const int wl = warp - 1;
+    const int pt = tid - 32;
     constexpr int kRopePieces = kBf16Rope ? 8 : 4;
-    const int n_cp = (4 - kTmaChunks) * 8 + (rope ? kRopePieces : 0);   // pieces a row
+    const int n_rp = rope ? kRopePieces : 0;           // 16-byte rope pieces a row
     const int row_bytes = kFmt == kDsMla ? kDsMlaRowBytes : p.d_qk;
     const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
-    const uint32_t tx_bytes = (uint32_t)(8 * kTmaChunks * 512);
-    int issued = 0;
-    for (int b = 0; b < nb; ++b) {
-      const int s = b & 1;
-      if (b >= kStages) W.wait(bar(kBarKvEmpty + s), ((b >> 1) - 1) & 1);
-      if (*abort_flag) break;                    // the stage may still be in use
-      __syncwarp();
-      issued = b + 1;
-      const uint32_t full = bar(kBarKvFull + s);
-      const uint32_t tile = sb + kOffTile + s * kStageBytes;
-      const int* bs = slots + b * kBK + 32 * wl;
-      if (kTmaChunks > 0 && elect_one()) {
-        mbar_arrive_expect_tx(full, tx_bytes);
-        for (int g = 0; g < 8; ++g) {
-          const int y0 = bs[4 * g], y1 = bs[4 * g + 1], y2 = bs[4 * g + 2], y3 = bs[4 * g + 3];
-          for (int c = 0; c < kTmaChunks; ++c)
-            tma_gather4(tile + c * kChunkBytes + (32 * wl + 4 * g) * 128, &a.kv_map, 128 * c, y0,
-                        y1, y2, y3, full);
+    int* slots = reinterpret_cast<int*>(sm + kOffSlot);
+    float* scs = reinterpret_cast<float*>(sm + kOffSc);
+    uint32_t* masks = reinterpret_cast<uint32_t*>(sm + kOffMask);
+    const uint32_t tx_bytes = (uint32_t)(8 * 4 * 512);
+    int g = 0, issued = 0;
+    bool stop = false;
+    for (int u = blockIdx.x; u < a.n_units && !stop; u += u_step) {
+      const UnitInfo ui = unit_info(a, u);
+      if (ui.nb == 0) continue;
+      // (the previous unit's gathers are all issued: the ids are free)
+      named_bar_sync(1, kProducers);
+      if (load_unit_slots(p, ui.t, ui.k0, ui.k1, ui.nb * kBK, slots, pt, kProducers))
+        atomicCAS(p.status, 0, kStatusBadIndex);
+      named_bar_sync(1, kProducers);
+      for (int j = 0; j < ui.nb; ++j, ++g) {
+        const int s = g & 1;
+        if (g >= kStages) W.wait(bar(kBarKvEmpty + s), ((g >> 1) - 1) & 1);
+        if (*abort_flag) {                       // the stage may still be in use
+          stop = true;
+          break;
         }
-      }
-      __syncwarp();
-      for (int e = lane; e < 32 * n_cp; e += 32) {
-        const int r = e / n_cp, k = e - r * n_cp;      // row of the warp, piece of the row
-        const int id = bs[r];
-        const int row = 32 * wl + r;
-        int c, u, src_off;
-        if (k < (4 - kTmaChunks) * 8) {
-          c = kTmaChunks + (k >> 3);
-          u = k & 7;
-          src_off = 128 * c + 16 * u;
-        } else {
-          c = 4;
-          u = k - (4 - kTmaChunks) * 8;
-          src_off = a.rope_x + 16 * u;
+        __syncwarp();
+        issued = g + 1;
+        const uint32_t full = bar(kBarKvFull + s);
+        const uint32_t tile = sb + kOffTile + s * kStageBytes;
+        const int* bs = slots + j * kBK + 32 * wl;
+        if (elect_one()) {
+          mbar_arrive_expect_tx(full, tx_bytes);
+          for (int q = 0; q < 8; ++q) {
+            const int y0 = bs[4 * q], y1 = bs[4 * q + 1], y2 = bs[4 * q + 2], y3 = bs[4 * q + 3];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              tma_gather4(tile + c * kChunkBytes + (32 * wl + 4 * q) * 128, &a.kv_map, 128 * c,
+                          y0, y1, y2, y3, full);
+          }
         }
-        const uint32_t dst =
-            tile + (uint32_t)(c * kChunkBytes + row * 128) + ((uint32_t)(u ^ (row & 7)) << 4);
-        const uint8_t* src = kv8 + (size_t)(id < 0 ? 0 : id) * row_bytes + src_off;
-        cp_async16(dst, src, id < 0 ? 0u : 16u);
+        __syncwarp();
+        for (int e = lane; e < 32 * n_rp; e += 32) {
+          const int r = e / n_rp, k = e - r * n_rp;      // row of the warp, rope piece
+          const int id = bs[r];
+          const int row = 32 * wl + r;
+          const uint32_t dst = tile + (uint32_t)(4 * kChunkBytes + row * 128) +
+                               ((uint32_t)(k ^ (row & 7)) << 4);
+          cp_async16(dst, kv8 + (size_t)(id < 0 ? 0 : id) * row_bytes + a.rope_x + 16 * k,
+                     id < 0 ? 0u : 16u);
+        }
+        cp_async_arrive_noinc(full);
+        // This thread's row: its valid bit and (group formats) its scales.
+        const int id = bs[lane];
+        const uint32_t m = __ballot_sync(0xffffffffu, id >= 0);
+        if (lane == 0) masks[s * 4 + wl] = m;
+        if (kGroup) {
+          float sc[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
+          if (id >= 0) {
+            if (kFmt == kDsMla) {
+              const float4 s4 = __ldg(reinterpret_cast<const float4*>(
+                  kv8 + (size_t)id * kDsMlaRowBytes + kDsMlaScaleOff));
+              sc[0] = s4.x; sc[1] = s4.y; sc[2] = s4.z; sc[3] = s4.w; sc[4] = 1.f;
+            } else if (kFmt == kE4m3Group4Kpe) {
+              const float4 s4 = __ldg(reinterpret_cast<const float4*>(p.k_scale + (int64_t)id * 4));
+              sc[0] = s4.x; sc[1] = s4.y; sc[2] = s4.z; sc[3] = s4.w; sc[4] = p.kpe_scale;
+            } else {
+              const float* r = p.k_scale + (int64_t)id * a.G;
+              sc[0] = __ldg(r); sc[1] = __ldg(r + 1); sc[2] = __ldg(r + 2); sc[3] = __ldg(r + 3);
+              if (a.G > 4) sc[4] = __ldg(r + 4);
+            }
+          }
+          float* dstf = scs + (s * kBK + pt) * kScaleRow;
+#pragma unroll
+          for (int q = 0; q < 5; ++q) dstf[q] = sc[q];
+        }
+        mbar_arrive(full);
       }
-      cp_async_arrive_noinc(full);
     }
     // Teardown: this thread's copies have landed; the gathers of the last
     // block issued into each stage too (earlier ones were consumed before the
     // stage was reissued).
     cp_async_wait_all();
-    if (kTmaChunks > 0 && lane == 0) {
+    if (lane == 0) {
       for (int b = issued - 1; b >= 0 && b >= issued - kStages; --b)
         W.drain(bar(kBarKvFull + (b & 1)), (b >> 1) & 1);
     }
@@ -451,29 +504,50 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
     const int wg = sw >> 2;                             // heads [8 wg, 8 wg + 8)
     const int q4 = warp & 3;                            // TMEM lane quarter
     const int key = 32 * q4 + lane;                     // tile row == TMEM lane
+    const int st = tid - 160;                           // 0..255
     const uint32_t lane_base = ((uint32_t)q4 * 32u) << 16;
     const int nbar_wg = 3 + wg;                         // warpgroup-local barrier
     float* qf_sh = reinterpret_cast<float*>(sm + kOffQf);
+    const float* scs = reinterpret_cast<const float*>(sm + kOffSc);
+    const uint32_t* masks = reinterpret_cast<const uint32_t*>(sm + kOffMask);
+    float* red = reinterpret_cast<float*>(sm + kOffRed) + wg * 32;      // [4 warps][8]
+    float* red_sc = reinterpret_cast<float*>(sm + kOffRedSc) + wg * 16; // [4 warps][4]
+    // This key's 128-byte row of the P' buffer (MN-major, 128-byte swizzle).
+    const uint32_t p_row = (uint32_t)(key >> 3) * 1024u + (uint32_t)(key & 7) * 128u;
+    const uint32_t p_sw = (uint32_t)(key & 7);
+    const float kscale = kFmt == kE4m3 ? __ldg(p.k_scale) : 1.f;
+    const float rope_cs = a.scale_log2;                 // bf16 rope: not scaled by 2^-a
 
-    // Q' = the QK B operand: rows [0, 16) = hi codes of heads h0.., rows
-    // [16, 32) = lo codes, K-major, 128-byte chunks of 32 rows, 128-byte
-    // swizzle.  Warp sw prepares heads 2 sw and 2 sw + 1.  For the 656-byte
-    // row the rope part of Q stays bf16, in chunk 4 (16 rows x 128 bytes).
-    if (nb > 0) {
+    // Q' = the QK B operand of unit ui: rows [0, 16) = hi codes of heads
+    // h0.., rows [16, 32) = lo codes, K-major, 128-byte chunks of 32 rows,
+    // 128-byte swizzle.  Warp sw prepares heads 2 sw and 2 sw + 1.  For the
+    // 656-byte row the rope part of Q stays bf16, in chunk 4 (16 rows x 128
+    // bytes).  Ends with the arrival on Q ready.
+    auto prepare_q = [&](const UnitInfo& ui) {
       const int n_fp8 = rope && !kBf16Rope ? 72 : 64;   // 8-channel pieces split to E4M3
       const int n_pc = rope ? 72 : 64;
-#pragma unroll 1
+      // both heads' loads first (one memory latency for the two)
+      uint4 x[2][3];
+#pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const int hl = 2 * sw + hh, hd = h0 + hl;
+        const int hd = ui.h0 + 2 * sw + hh;
         const bool live = hd < p.h;
-        uint4 x[3];
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+          const int k = lane + 32 * j;
+          x[hh][j] = (live && k < n_pc) ? __ldg(q_chunk(p, ui.t, hd, 8 * k))
+                                        : make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int hl = 2 * sw + hh;
         float mx = 0.f;
 #pragma unroll
         for (int j = 0; j < 3; ++j) {
           const int k = lane + 32 * j;
-          x[j] = (live && k < n_pc) ? __ldg(q_chunk(p, t, hd, 8 * k)) : make_uint4(0u, 0u, 0u, 0u);
           if (k < n_fp8) {
-            const uint32_t w[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+            const uint32_t w[4] = {x[hh][j].x, x[hh][j].y, x[hh][j].z, x[hh][j].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e)
               mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[e] << 16)),
@@ -492,7 +566,7 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
         for (int j = 0; j < 3; ++j) {
           const int k = lane + 32 * j;
           if (k < n_fp8) {
-            const uint32_t w[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+            const uint32_t w[4] = {x[hh][j].x, x[hh][j].y, x[hh][j].z, x[hh][j].w};
             float f[8];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -510,290 +584,361 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
           } else if (kBf16Rope && k < n_pc) {
             const int u = k - 64;                           // 16-byte unit of the bf16 row
             *reinterpret_cast<uint4*>(sm + kOffQ + 4 * kQChunkBytes + hl * 128 +
-                                      ((u ^ (hl & 7)) << 4)) = x[j];
+                                      ((u ^ (hl & 7)) << 4)) = x[hh][j];
           }
         }
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(kBarQReady));
-    }
-    named_bar_sync(5, kSoftmax);                        // qf_sh written
-    // Per head of this warpgroup: Q factor 2^-a, folded with the score scale
-    // (and the per-tensor E4M3 scale).
-    const float kscale = kFmt == kE4m3 ? __ldg(p.k_scale) : 1.f;
-    float cs[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) cs[i] = qf_sh[8 * wg + i] * a.scale_log2 * kscale;
-    const float rope_cs = a.scale_log2;                 // bf16 rope: not scaled by 2^-a
-    bool head_ok[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) head_ok[i] = h0 + 8 * wg + i < p.h;
-
-    float m_run[8], l_part[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) { m_run[i] = -INFINITY; l_part[i] = 0.f; }
-    float R[4] = {0.f, 0.f, 0.f, 0.f};                  // PV group factors (0: not set)
-    float* red = reinterpret_cast<float*>(sm + kOffRed) + wg * 32;      // [4 warps][8]
-    float* red_sc = reinterpret_cast<float*>(sm + kOffRedSc) + wg * 16; // [4 warps][4]
-    // This key's 128-byte row of a P' buffer (MN-major, 128-byte swizzle).
-    const uint32_t p_row = (uint32_t)(key >> 3) * 1024u + (uint32_t)(key & 7) * 128u;
-    const uint32_t p_sw = (uint32_t)(key & 7);
-    const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
-
-    // The key's group scales of block b (0 when masked): [0..3] the ckv
-    // groups, [4] the rope group.
-    auto load_scales = [&](int b, float (&sc)[5]) {
-      const int id = b < nb ? slots[b * kBK + key] : -1;
-#pragma unroll
-      for (int g = 0; g < 5; ++g) sc[g] = 0.f;
-      if (!kGroup || id < 0) return;
-      if (kFmt == kDsMla) {
-        const float4 s4 = __ldg(reinterpret_cast<const float4*>(kv8 + (size_t)id * kDsMlaRowBytes +
-                                                               kDsMlaScaleOff));
-        sc[0] = s4.x; sc[1] = s4.y; sc[2] = s4.z; sc[3] = s4.w; sc[4] = 1.f;
-      } else if (kFmt == kE4m3Group4Kpe) {
-        const float* r = p.k_scale + (int64_t)id * 4;
-        sc[0] = __ldg(r); sc[1] = __ldg(r + 1); sc[2] = __ldg(r + 2); sc[3] = __ldg(r + 3);
-        sc[4] = p.kpe_scale;
-      } else {
-        const float* r = p.k_scale + (int64_t)id * a.G;
-        sc[0] = __ldg(r); sc[1] = __ldg(r + 1); sc[2] = __ldg(r + 2); sc[3] = __ldg(r + 3);
-        if (a.G > 4) sc[4] = __ldg(r + 4);
+    };
+    // The next unit of this CTA with at least one block (n_units: none).
+    auto next_unit = [&](int u) {
+      for (u += u_step; u < a.n_units; u += u_step)
+        if (unit_info(a, u).nb > 0) break;
+      return u;
+    };
+    // Its q rows into L2 (144 lines of 128 bytes for 16 heads of 576 channels).
+    auto prefetch_q = [&](int u) {
+      if (u >= a.n_units) return;
+      const UnitInfo ui = unit_info(a, u);
+      for (int i = st; i < kHeads * 9; i += kSoftmax) {
+        const int hd = ui.h0 + i / 9, line = i % 9;
+        if (hd < p.h && 64 * line < p.d_qk) prefetch_l2(q_chunk(p, ui.t, hd, 64 * line));
       }
     };
-    float nsc[5];
-    load_scales(0, nsc);
-
-    for (int b = 0; b < nb; ++b) {
-      const int s = b & 1;
-      float sc[5];
+    auto write_empty = [&](const UnitInfo& ui) {
+      // O = 0 and LSE = -inf for the unit's heads (channel `key` of each
+      // 128-channel block; thread key < 8 the LSE of head 8 wg + key).
+#pragma unroll 1
+      for (int i = 0; i < 8; ++i) {
+        const int hd = ui.h0 + 8 * wg + i;
+        if (hd >= p.h) break;
+        const int64_t orow = (int64_t)ui.t * p.h + hd;
 #pragma unroll
-      for (int g = 0; g < 5; ++g) sc[g] = nsc[g];
-      load_scales(b + 1, nsc);                          // next block's, in flight
-      W.wait(bar(kBarSFull + s), (b >> 1) & 1);
-      __syncwarp();
-      tc_fence_after();
-      // a4 result: per group, this warpgroup's 8 heads hi (columns 8 wg..)
-      // and lo (16 + 8 wg..).
-      float sp[8];
-      {
-        const uint32_t c0 = tmem + lane_base + kColS + kSBuf * s + 8u * (uint32_t)wg;
-        if (kGroup) {
-          uint32_t w[5][2][8];
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            tmem_ld8(c0 + kNq * g, w[g][0]);
-            tmem_ld8(c0 + kNq * g + 16, w[g][1]);
-          }
-          if (rope) {
-            tmem_ld8(c0 + kNq * 4, w[4][0]);
-            if (!kBf16Rope) tmem_ld8(c0 + kNq * 4 + 16, w[4][1]);
-          }
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            float acc = 0.f;
-#pragma unroll
-            for (int g = 0; g < 4; ++g)
-              acc = fmaf(sc[g], fmaf(__uint_as_float(w[g][1][i]), 0.0625f,
-                                     __uint_as_float(w[g][0][i])), acc);
-            float r = 0.f;
-            if (rope && !kBf16Rope)
-              acc = fmaf(sc[4], fmaf(__uint_as_float(w[4][1][i]), 0.0625f,
-                                     __uint_as_float(w[4][0][i])), acc);
-            if (rope && kBf16Rope) r = __uint_as_float(w[4][0][i]);
-            sp[i] = fmaf(acc, cs[i], r * rope_cs);
-          }
-        } else {
-          uint32_t w0[8], w1[8];
-          tmem_ld8(c0, w0);
-          tmem_ld8(c0 + 16, w1);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            sp[i] = fmaf(__uint_as_float(w1[i]), 0.0625f, __uint_as_float(w0[i])) * cs[i];
+        for (int c = 0; c < 4; ++c) {
+          const int ch = 128 * c + key;
+          if (p.fp32_out)
+            p.o_part[((int64_t)ui.split * p.T * p.h + orow) * p.d_v + ch] = 0.f;
+          else
+            reinterpret_cast<__nv_bfloat16*>(p.out)[orow * p.d_v + ch] = __float2bfloat16_rn(0.f);
         }
       }
-      tc_fence_before();
-      mbar_arrive(bar(kBarSEmpty + s));
+      if (key < 8 && ui.h0 + 8 * wg + key < p.h) {
+        const int64_t orow = (int64_t)ui.t * p.h + ui.h0 + 8 * wg + key;
+        if (p.fp32_out)
+          p.lse_part[(int64_t)ui.split * p.T * p.h + orow] = -INFINITY;
+        else if (p.lse)
+          p.lse[orow] = -INFINITY;
+      }
+    };
 
-      // a5: masked scores (log2 units) and the lazy running max; with group
-      // scales also the lazy PV group factors R (scale * R <= 1).
-      const bool key_ok = ((masks[b * 4 + (key >> 5)] >> (key & 31)) & 1u) != 0u;
-      bool need = false;
+    int g = 0, ku = 0;
+    int u = blockIdx.x;
+    while (u < a.n_units && unit_info(a, u).nb == 0) {   // leading empty units
+      write_empty(unit_info(a, u));
+      u += u_step;
+    }
+    if (u < a.n_units) prepare_q(unit_info(a, u));
+    while (u < a.n_units) {
+      const UnitInfo ui = unit_info(a, u);
+      const int un = next_unit(u);
+      prefetch_q(un);
+      named_bar_sync(5, kSoftmax);                      // qf_sh of this unit written
+      // Per head of this warpgroup: Q factor 2^-a, folded with the score
+      // scale (and the per-tensor E4M3 scale).
+      float cs[8];
+      bool head_ok[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        sp[i] = (key_ok && head_ok[i]) ? sp[i] : -INFINITY;
-        need |= sp[i] > m_run[i] + kT;
+        cs[i] = qf_sh[8 * wg + i] * a.scale_log2 * kscale;
+        head_ok[i] = ui.h0 + 8 * wg + i < p.h;
       }
-      if (kGroup) {
+      float m_run[8], l_part[8];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) need |= R[g] == 0.f || sc[g] * R[g] > 1.f;
-      }
-      float alpha[8], ratio[4] = {1.f, 1.f, 1.f, 1.f};
+      for (int i = 0; i < 8; ++i) { m_run[i] = -INFINITY; l_part[i] = 0.f; }
+      float R[4] = {0.f, 0.f, 0.f, 0.f};                // PV group factors (0: not set)
+
+      for (int j = 0; j < ui.nb; ++j, ++g) {
+        const int s = g & 1;
+        // the block's valid bits and scales (stage s), then its scores
+        W.wait(bar(kBarKvFull + s), (g >> 1) & 1);
+        float sc[5];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) alpha[i] = 1.f;
-      const bool voted = named_bar_or(2, kSoftmax, need);
-      if (voted) {
-        float bm[8];
+        for (int q = 0; q < 5; ++q) sc[q] = kGroup ? scs[(s * kBK + key) * kScaleRow + q] : 0.f;
+        const bool key_ok = ((masks[s * 4 + (key >> 5)] >> (key & 31)) & 1u) != 0u;
+        W.wait(bar(kBarSFull + s), (g >> 1) & 1);
+        __syncwarp();
+        tc_fence_after();
+        // a4 result: per group, this warpgroup's 8 heads hi (columns 8 wg..)
+        // and lo (16 + 8 wg..).
+        float sp[8];
+        {
+          const uint32_t c0 = tmem + lane_base + kColS + kSBuf * s + 8u * (uint32_t)wg;
+          if (kGroup) {
+            // two batches of TMEM loads (register budget): groups 0, 1, then
+            // groups 2, 3 and the rope
+            float acc[8];
+            {
+              uint32_t w[2][2][8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) bm[i] = sp[i];
-        const float wmax = xreduce8<true>(bm, lane);
-        if ((lane & 17) == 0) red[q4 * 8 + ((lane >> 1) & 7)] = wmax;
-        if (kGroup) {
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            float x = sc[g];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-            if (lane == 0) red_sc[q4 * 4 + g] = x;
-          }
-        }
-        named_bar_sync(nbar_wg, 128);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float bmax = fmaxf(fmaxf(red[i], red[8 + i]), fmaxf(red[16 + i], red[24 + i]));
-          if (bmax > m_run[i] + kT) {             // also true for the first finite max
-            alpha[i] = ex2_approx(m_run[i] - bmax);   // 0 when m_run = -inf
-            m_run[i] = bmax;
-          }
-        }
-        if (kGroup) {
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const float ms = fmaxf(fmaxf(red_sc[g], red_sc[4 + g]),
-                                   fmaxf(red_sc[8 + g], red_sc[12 + g]));
-            if (ms > 0.f && (R[g] == 0.f || ms * R[g] > 1.f)) {
-              const float rn = pow2_at_most_inv(ms);
-              if (R[g] != 0.f) ratio[g] = rn / R[g];
-              R[g] = rn;
-            }
-          }
-        }
-        named_bar_sync(nbar_wg, 128);             // red may be rewritten
-      }
-      float pe[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        pe[i] = m_run[i] == -INFINITY ? 0.f : ex2_approx(sp[i] - m_run[i]);
-        l_part[i] = fmaf(l_part[i], alpha[i], pe[i]);
-      }
-      // a6 operand: P' hi / lo codes into buffer s (per group with scales).
-      if (b >= 2) W.wait(bar(kBarPEmpty + s), ((b >> 1) - 1) & 1);   // PV(b-2) read it
-      uint8_t* prow = sm + kOffP + s * kPBytes + p_row;
-#pragma unroll
-      for (int g = 0; g < (kGroup ? 4 : 1); ++g) {
-        const float f = kGroup ? sc[g] * R[g] * kPShift : kPShift;
-        float x[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = pe[i] * f;
-        uint2 hi, lo;
-        split8(x, hi, lo);
-        *reinterpret_cast<uint2*>(prow + ((((uint32_t)(2 * g) ^ p_sw) << 4) | (8u * wg))) = hi;
-        *reinterpret_cast<uint2*>(prow + ((((uint32_t)(2 * g + 1) ^ p_sw) << 4) | (8u * wg))) = lo;
-      }
-      fence_proxy_async_smem();
-      if (voted && b >= 1) {
-        // O^T row (channel `key` of each 128-channel block): this
-        // warpgroup's head columns (hi and lo) *= alpha * ratio of the block.
-        bool any = false;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) any |= alpha[i] != 1.f;
-#pragma unroll
-        for (int g = 0; g < 4; ++g) any |= ratio[g] != 1.f;
-        if (any) {                                      // uniform in the warpgroup
-          W.wait(bar(kBarODone), (b - 1) & 1);
-          __syncwarp();
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-              const uint32_t col = tmem + lane_base + kColO + 32u * c + 16u * part + 8u * wg;
-              uint32_t w[8];
-              tmem_ld8(col, w);
+              for (int gg = 0; gg < 2; ++gg) {
+                tmem_ld8(c0 + kNq * gg, w[gg][0]);
+                tmem_ld8(c0 + kNq * gg + 16, w[gg][1]);
+              }
               tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 8; ++i)
-                w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha[i] * ratio[c]);
-              tmem_st8(col, w);
+              for (int i = 0; i < 8; ++i) {
+                acc[i] = sc[0] * fmaf(__uint_as_float(w[0][1][i]), 0.0625f, __uint_as_float(w[0][0][i]));
+                acc[i] = fmaf(sc[1], fmaf(__uint_as_float(w[1][1][i]), 0.0625f,
+                                          __uint_as_float(w[1][0][i])), acc[i]);
+              }
+            }
+            {
+              uint32_t w[3][2][8];
+#pragma unroll
+              for (int gg = 0; gg < 2; ++gg) {
+                tmem_ld8(c0 + kNq * (gg + 2), w[gg][0]);
+                tmem_ld8(c0 + kNq * (gg + 2) + 16, w[gg][1]);
+              }
+              if (rope) {
+                tmem_ld8(c0 + kNq * 4, w[2][0]);
+                if (!kBf16Rope) tmem_ld8(c0 + kNq * 4 + 16, w[2][1]);
+              }
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+#pragma unroll
+                for (int gg = 0; gg < 2; ++gg)
+                  acc[i] = fmaf(sc[gg + 2], fmaf(__uint_as_float(w[gg][1][i]), 0.0625f,
+                                                 __uint_as_float(w[gg][0][i])), acc[i]);
+                float r = 0.f;
+                if (rope && !kBf16Rope)
+                  acc[i] = fmaf(sc[4], fmaf(__uint_as_float(w[2][1][i]), 0.0625f,
+                                            __uint_as_float(w[2][0][i])), acc[i]);
+                if (rope && kBf16Rope) r = __uint_as_float(w[2][0][i]);
+                sp[i] = fmaf(acc[i], cs[i], r * rope_cs);
+              }
+            }
+          } else {
+            uint32_t w0[8], w1[8];
+            tmem_ld8(c0, w0);
+            tmem_ld8(c0 + 16, w1);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              sp[i] = fmaf(__uint_as_float(w1[i]), 0.0625f, __uint_as_float(w0[i])) * cs[i];
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar(kBarSEmpty + s));
+
+        // a5: masked scores (log2 units) and the lazy running max; with group
+        // scales also the lazy PV group factors R (scale * R <= 1).
+        bool need = false;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          sp[i] = (key_ok && head_ok[i]) ? sp[i] : -INFINITY;
+          need |= sp[i] > m_run[i] + kT;
+        }
+        if (kGroup) {
+#pragma unroll
+          for (int gg = 0; gg < 4; ++gg) need |= R[gg] == 0.f || sc[gg] * R[gg] > 1.f;
+        }
+        float alpha[8], ratio[4] = {1.f, 1.f, 1.f, 1.f};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) alpha[i] = 1.f;
+        const bool voted = named_bar_or(2, kSoftmax, need);
+        if (voted) {
+          float bm[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) bm[i] = sp[i];
+          const float wmax = xreduce8<true>(bm, lane);
+          if ((lane & 17) == 0) red[q4 * 8 + ((lane >> 1) & 7)] = wmax;
+          if (kGroup) {
+#pragma unroll
+            for (int gg = 0; gg < 4; ++gg) {
+              float x = sc[gg];
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+              if (lane == 0) red_sc[q4 * 4 + gg] = x;
             }
           }
-          tmem_wait_st();
+          named_bar_sync(nbar_wg, 128);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float bmax = fmaxf(fmaxf(red[i], red[8 + i]), fmaxf(red[16 + i], red[24 + i]));
+            if (bmax > m_run[i] + kT) {             // also true for the first finite max
+              alpha[i] = ex2_approx(m_run[i] - bmax);   // 0 when m_run = -inf
+              m_run[i] = bmax;
+            }
+          }
+          if (kGroup) {
+#pragma unroll
+            for (int gg = 0; gg < 4; ++gg) {
+              const float ms = fmaxf(fmaxf(red_sc[gg], red_sc[4 + gg]),
+                                     fmaxf(red_sc[8 + gg], red_sc[12 + gg]));
+              if (ms > 0.f && (R[gg] == 0.f || ms * R[gg] > 1.f)) {
+                const float rn = pow2_at_most_inv(ms);
+                if (R[gg] != 0.f) ratio[gg] = rn / R[gg];
+                R[gg] = rn;
+              }
+            }
+          }
+          named_bar_sync(nbar_wg, 128);             // red may be rewritten
         }
+        float pe[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          pe[i] = m_run[i] == -INFINITY ? 0.f : ex2_approx(sp[i] - m_run[i]);
+          l_part[i] = fmaf(l_part[i], alpha[i], pe[i]);
+        }
+        // a6 operand: P' hi / lo codes (per group with scales).
+        if (g >= 1) W.wait(bar(kBarPEmpty), (g - 1) & 1);   // PV(g-1) read it
+        uint8_t* prow = sm + kOffP + p_row;
+#pragma unroll
+        for (int gg = 0; gg < (kGroup ? 4 : 1); ++gg) {
+          const float f = kGroup ? sc[gg] * R[gg] * kPShift : kPShift;
+          float x[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[i] = pe[i] * f;
+          uint2 hi, lo;
+          split8(x, hi, lo);
+          *reinterpret_cast<uint2*>(prow + ((((uint32_t)(2 * gg) ^ p_sw) << 4) | (8u * wg))) = hi;
+          *reinterpret_cast<uint2*>(prow + ((((uint32_t)(2 * gg + 1) ^ p_sw) << 4) | (8u * wg))) =
+              lo;
+        }
+        fence_proxy_async_smem();
+        if (voted && j >= 1) {
+          // O^T row (channel `key` of each 128-channel block): this
+          // warpgroup's head columns (hi and lo) *= alpha * ratio of the block.
+          bool any = false;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) any |= alpha[i] != 1.f;
+#pragma unroll
+          for (int gg = 0; gg < 4; ++gg) any |= ratio[gg] != 1.f;
+          if (any) {                                      // uniform in the warpgroup
+            W.wait(bar(kBarODone), (g - 1) & 1);
+            __syncwarp();
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+#pragma unroll
+              for (int part = 0; part < 2; ++part) {
+                const uint32_t col = tmem + lane_base + kColO + 32u * c + 16u * part + 8u * wg;
+                uint32_t w[8];
+                tmem_ld8(col, w);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha[i] * ratio[c]);
+                tmem_st8(col, w);
+              }
+            }
+            tmem_wait_st();
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar(kBarPFull));
       }
-      tc_fence_before();
-      mbar_arrive(bar(kBarPFull + s));
-    }
+      // This unit's QK MMAs are done (its last scores were read): Q' of the
+      // next unit can be written now, so that its first QK runs during this
+      // unit's epilogue.
+      if (un < a.n_units) prepare_q(unit_info(a, un));
 
-    // ---- a7: epilogue ---------------------------------------------------------
-    // Row sums: reduce the per-key partial sums over the block's keys.
-    float l_tot[8];
-    {
-      float l8[8];
+      // ---- a7: epilogue -------------------------------------------------------
+      // Row sums: reduce the per-key partial sums over the block's keys.
+      float l_tot[8];
+      {
+        float l8[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) l8[i] = l_part[i];
-      const float ws = xreduce8<false>(l8, lane);
-      named_bar_sync(nbar_wg, 128);
-      if ((lane & 17) == 0) red[q4 * 8 + ((lane >> 1) & 7)] = ws;
-      named_bar_sync(nbar_wg, 128);
+        for (int i = 0; i < 8; ++i) l8[i] = l_part[i];
+        const float ws = xreduce8<false>(l8, lane);
+        named_bar_sync(nbar_wg, 128);
+        if ((lane & 17) == 0) red[q4 * 8 + ((lane >> 1) & 7)] = ws;
+        named_bar_sync(nbar_wg, 128);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) l_tot[i] = (red[i] + red[8 + i]) + (red[16 + i] + red[24 + i]);
-    }
-    if (nb > 0) {
-      W.wait(bar(kBarOFinal), 0);
+        for (int i = 0; i < 8; ++i) l_tot[i] = (red[i] + red[8 + i]) + (red[16 + i] + red[24 + i]);
+      }
+      W.wait(bar(kBarOFinal), ku & 1);
       __syncwarp();
       tc_fence_after();
-    }
-    const float oscale = kFmt == kE4m3 ? kscale : 1.f;
-#pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      uint32_t wh[8], wl8[8];
+      const float oscale = kFmt == kE4m3 ? kscale : 1.f;
+      float inv[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) { wh[i] = 0u; wl8[i] = 0u; }
-      __syncwarp();
-      if (nb > 0) {
+      for (int i = 0; i < 8; ++i) inv[i] = l_tot[i] > 0.f ? oscale / (l_tot[i] * kPShift) : 0.f;
+      // bf16 O goes through the staging rows [16 heads][512] and leaves as
+      // one bulk copy (the token's rows of these heads are contiguous); the
+      // previous unit's copy has read the staging rows before they are
+      // rewritten.  fp32 partials are stored directly.
+      __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + kOffOst);
+      if (!p.fp32_out) {
+        if (st == 0) bulk_wait_read_all();
+        named_bar_sync(5, kSoftmax);
+      }
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t wh[8], wl8[8];
+        __syncwarp();
         const uint32_t col = tmem + lane_base + kColO + 32u * c + 8u * wg;
         tmem_ld8(col, wh);
         tmem_ld8(col + 16, wl8);
         tmem_wait_ld();
-      }
-      const float rc = kGroup ? R[c] : 1.f;
-      const int ch = 128 * c + key;                   // output channel of lane `key`
+        const float rc = kGroup ? R[c] : 1.f;
+        const float rinv = rc > 0.f ? 1.f / rc : 0.f;
+        const int ch = 128 * c + key;                   // output channel of lane `key`
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (head_ok[i]) {
-          const bool empty = !(l_tot[i] > 0.f) || nb == 0 || !(rc > 0.f);
-          const float o = empty ? 0.f
-                                : fmaf(__uint_as_float(wl8[i]), 0.0625f, __uint_as_float(wh[i])) *
-                                      (oscale / (l_tot[i] * kPShift * rc));
-          const int64_t orow = (int64_t)t * p.h + h0 + 8 * wg + i;
-          if (p.fp32_out)
-            p.o_part[((int64_t)split * p.T * p.h + orow) * p.d_v + ch] = o;
-          else
-            reinterpret_cast<__nv_bfloat16*>(p.out)[orow * p.d_v + ch] = __float2bfloat16_rn(o);
+        for (int i = 0; i < 8; ++i) {
+          // (no valid key for the head, or none with a nonzero scale in this
+          // group: 0 exactly)
+          const float o = (inv[i] > 0.f && rinv > 0.f)
+                              ? fmaf(__uint_as_float(wl8[i]), 0.0625f, __uint_as_float(wh[i])) *
+                                    (inv[i] * rinv)
+                              : 0.f;
+          if (!p.fp32_out) {
+            ost[(8 * wg + i) * 512 + ch] = __float2bfloat16_rn(o);
+          } else if (head_ok[i]) {
+            const int64_t orow = (int64_t)ui.t * p.h + ui.h0 + 8 * wg + i;
+            p.o_part[((int64_t)ui.split * p.T * p.h + orow) * p.d_v + ch] = o;
+          }
         }
       }
-    }
-    // Thread `key` < 8 writes the LSE of head 8 wg + key.
-    if (key < 8 && h0 + 8 * wg + key < p.h) {
-      float mi = m_run[0], li = l_tot[0];
-#pragma unroll
-      for (int i = 1; i < 8; ++i) {
-        mi = key == i ? m_run[i] : mi;
-        li = key == i ? l_tot[i] : li;
+      // (the TMEM loads of O are complete: the next unit's first PV, which
+      // waits for this thread's next P' hand-off, may overwrite it)
+      tc_fence_before();
+      if (!p.fp32_out) {
+        fence_proxy_async_smem();
+        named_bar_sync(5, kSoftmax);
+        if (st == 0) {
+          const int nh = min(kHeads, p.h - ui.h0);
+          bulk_store(reinterpret_cast<__nv_bfloat16*>(p.out) + ((int64_t)ui.t * p.h + ui.h0) * 512,
+                     sb + kOffOst, (uint32_t)(nh * 1024));
+          bulk_commit_group();
+        }
       }
-      const bool empty = !(li > 0.f) || nb == 0;
-      const float lse_v = empty ? -INFINITY : (mi + log2f(li)) * 0.69314718055994530942f;
-      const int64_t orow = (int64_t)t * p.h + h0 + 8 * wg + key;
-      if (p.fp32_out)
-        p.lse_part[(int64_t)split * p.T * p.h + orow] = lse_v;
-      else if (p.lse)
-        p.lse[orow] = lse_v;
+      // Thread `key` < 8 writes the LSE of head 8 wg + key.
+      if (key < 8 && ui.h0 + 8 * wg + key < p.h) {
+        float mi = m_run[0], li = l_tot[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) {
+          mi = key == i ? m_run[i] : mi;
+          li = key == i ? l_tot[i] : li;
+        }
+        const bool empty = !(li > 0.f);
+        const float lse_v = empty ? -INFINITY : (mi + log2f(li)) * 0.69314718055994530942f;
+        const int64_t orow = (int64_t)ui.t * p.h + ui.h0 + 8 * wg + key;
+        if (p.fp32_out)
+          p.lse_part[(int64_t)ui.split * p.T * p.h + orow] = lse_v;
+        else if (p.lse)
+          p.lse[orow] = lse_v;
+      }
+      ++ku;
+      // the empty units up to the next one with blocks
+      for (u += u_step; u < un; u += u_step) write_empty(unit_info(a, u));
     }
   }
 
   // ---- teardown -------------------------------------------------------------
+  if (tid == 160) bulk_wait_all();                // the O copies have been written
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -850,8 +995,11 @@ cudaError_t launch_tc_fp8(const FwdParams& p, cudaStream_t stream) {
   a.rope_x = p.kv_format == kDsMla ? kDsMlaRopeOff : 512;
   a.G = (p.d_qk + 127) / 128;
   a.scale_log2 = p.sm_scale * 1.4426950408889634f;
-  const int64_t blocks = (int64_t)p.T * p.splits * a.n_hg;   // one CTA per unit
-  if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  const int64_t units = (int64_t)p.T * p.splits * a.n_hg;
+  if (units > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  a.n_units = (int)units;
+  // persistent: one CTA per SM (the shared memory allows no second one)
+  const int64_t blocks = units < p.num_sms ? units : (p.num_sms > 0 ? p.num_sms : 1);
   switch (p.kv_format) {
     case kE4m3: return launch_fmt<kE4m3>(a, (unsigned)blocks, stream);
     case kE4m3Group: return launch_fmt<kE4m3Group>(a, (unsigned)blocks, stream);

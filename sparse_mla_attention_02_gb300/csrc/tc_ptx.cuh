@@ -161,6 +161,13 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t
       "r"(src_cta), "r"(bytes), "r"(bar_cluster)
       : "memory");
 }
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to
+// global memory, tracked by the bulk-group of this thread.
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src_cta, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"(src_cta), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
