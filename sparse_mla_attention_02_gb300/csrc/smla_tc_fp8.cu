@@ -153,24 +153,26 @@ constexpr uint32_t idesc_e4m3(int M, int N, bool a_mn_major, bool b_mn_major) {
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// Two floats -> two E4M3 codes (round to nearest even, saturating), a in the
-// low byte; and two E4M3 codes back to floats (exact).
-__device__ __forceinline__ uint32_t e4m3x2_of(float a, float b) {
-  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+// Split x0..x7 (|x| <= 448) into hi = E4M3(x) and lo = E4M3(16 (x - hi)),
+// eight codes each (x0 in the lowest byte).  The pairs go through f16: x is
+// rounded to f16 first (2^-11 relative, below the pair's 2^-8), and x - hi
+// and its product by 16 are exact in f16.
+__device__ __forceinline__ uint32_t e4m3x2_of_h2(__half2 h) {
+  return (uint32_t)__nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&h),
+                                              __NV_SATFINITE, __NV_E4M3);
 }
-__device__ __forceinline__ float2 f2_of_e4m3x2(uint32_t v) {
+__device__ __forceinline__ __half2 h2_of_e4m3x2(uint32_t v) {
   const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)v, __NV_E4M3);
-  return __half22float2(*reinterpret_cast<const __half2*>(&r));
+  return *reinterpret_cast<const __half2*>(&r);
 }
-// Split x0..x7 into hi = E4M3(x) and lo = E4M3(16 (x - hi)), eight codes
-// each (x0 in the lowest byte).
 __device__ __forceinline__ void split8(const float (&x)[8], uint2& hi, uint2& lo) {
   uint32_t h[4], l[4];
+  const __half2 k16 = __float2half2_rn(16.f);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    h[k] = e4m3x2_of(x[2 * k], x[2 * k + 1]);
-    const float2 f = f2_of_e4m3x2(h[k]);
-    l[k] = e4m3x2_of((x[2 * k] - f.x) * 16.f, (x[2 * k + 1] - f.y) * 16.f);
+    const __half2 xh = __floats2half2_rn(x[2 * k], x[2 * k + 1]);
+    h[k] = e4m3x2_of_h2(xh);
+    l[k] = e4m3x2_of_h2(__hmul2(__hsub2(xh, h2_of_e4m3x2(h[k])), k16));
   }
   hi = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
   lo = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
