@@ -132,7 +132,9 @@ static_assert(kOffQStage + 128 * kQStageRow <= kOffTile + kStages * kTileBytes, 
 struct TcArgs {
   CUtensorMap kv_map;  // bf16 cache as a 2-D tensor [num_slots, d_qk], 64-channel boxes
   CUtensorMap q_map;   // q as a 2-D tensor [T * 128, d_qk], 64-channel x 128-row boxes
+  CUtensorMap o_map;   // out as a 2-D tensor [T * 128, 512], 64-channel x 128-row boxes
   int q_tma;           // 1: Q staged by TMA boxes (bf16 cache, h = 128, q concatenated)
+  int o_tma;           // 1: O leaves by TMA boxes (h = 128, bf16 out)
   FwdParams p;
   int fp8;          // 1: E4M3 cache with a per-tensor scale (converted on load)
   int g_lo[2];      // first cache channel gathered by CTA r
@@ -673,12 +675,50 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
       tc_fence_after();
     }
     const bool empty = !(l_tot > 0.f) || nb == 0;
-    const float inv = empty ? 0.f : kscale / l_tot;
+    const float inv = empty ? 0.f : __fdividef(kscale, l_tot);   // (IEEE division: slow here)
     const bool live = head < p.h;          // pad rows past h are not written
     const int64_t orow = (int64_t)t * p.h + (live ? head : 0);
     // Every lane of the warpgroup runs the TMEM loads (warp-collective);
     // only the stores depend on the lane's head.  Warpgroup wg writes output
     // channels [256 r + 128 wg, 256 r + 128 wg + 128).
+    if (a.o_tma) {
+      // bf16 O through two 128-byte-swizzled boxes of 64 channels x 128 head
+      // rows in the gather stages (idle now: every gather was consumed), then
+      // two TMA stores issued by the warpgroup's first thread (one row of a
+      // box per thread: the stores are whole 128-byte lines; a thread's own
+      // 16-byte stores would each touch half a sector of a different row).
+      uint8_t* box0 = sm + kOffTile + (uint32_t)(2 * wg) * 16384u + (uint32_t)head * 128u;
+      const uint32_t hsw = (uint32_t)head & 7u;
+#pragma unroll 1
+      for (int c = 0; c < 128; c += 16) {
+        uint32_t w[16];
+        __syncwarp();
+        if (nb > 0) {
+          tmem_ld16(tmem + lane_base + kColO + 128 * wg + c, w);
+          tmem_wait_ld();
+        }
+        uint32_t o[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          o[k] = empty ? 0u
+                       : pack_bf16(__uint_as_float(w[2 * k]) * inv,
+                                   __uint_as_float(w[2 * k + 1]) * inv);
+        const uint32_t ck = (uint32_t)(c >> 3);             // 16-byte chunk of the 128 channels
+        uint8_t* brow = box0 + (ck >> 3) * 16384u;
+        *reinterpret_cast<uint4*>(brow + ((((ck & 7u) + 0u) ^ hsw) << 4)) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(brow + ((((ck & 7u) + 1u) ^ hsw) << 4)) =
+            make_uint4(o[4], o[5], o[6], o[7]);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(nbar, 128);
+      if (wlead) {
+        for (int bx = 0; bx < 2; ++bx)
+          tma_store_2d(&a.o_map, sb + kOffTile + (uint32_t)(2 * wg + bx) * 16384u,
+                       256 * (int)r + 128 * wg + 64 * bx, t * 128);
+        bulk_commit_group();
+      }
+    } else {
 #pragma unroll 1
     for (int c = 128 * wg; c < 128 * wg + 128; c += 16) {
       uint32_t w[16];
@@ -710,6 +750,7 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
         *reinterpret_cast<uint4*>(dst + 8) = make_uint4(o[4], o[5], o[6], o[7]);
       }
     }
+    }
     // Both CTAs hold the same LSE; the first warpgroup of CTA r writes heads
     // [64r, 64r + 64).
     if (wg == 0 && live && (uint32_t)(i >> 6) == r) {
@@ -728,7 +769,8 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
   // barriers first.
   // (also after an abort: the peer's shared memory stays until the cluster
   // barrier below, which this CTA passes only after its copies are complete)
-  if ((tid == 128 || tid == 256) && nb > 0) bulk_wait_all();
+  // (and the O boxes' TMA stores have read the staging)
+  if (tid == 128 || tid == 256) bulk_wait_all();
   if (tid == 0 && a.q_tma) W.drain(bar(kBarQLoaded), 0);
   if (tid == 128 && nb > 0) {
     if (nb >= 2) W.wait(bar(kBarXFree + ((nb - 2) & 1)), ((nb - 2) >> 1) & 1);
@@ -808,6 +850,22 @@ cudaError_t launch_tc(const FwdParams& p, cudaStream_t stream) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
     a.q_tma = 1;
+  }
+  // O by TMA boxes: 128 heads (a token's rows are exactly one box high),
+  // bf16 output.
+  if (p.h == 128 && !p.fp32_out) {
+    auto encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)p.d_v, (cuuint64_t)p.T * 128};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.d_v * 2};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&a.o_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.out, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    a.o_tma = 1;
   }
   if (p.d_qk == 576) {
     a.g_lo[0] = 0;   a.n_boxes[0] = 5; a.qk_lo[0] = 0;  a.q_lo[0] = 0;

@@ -151,6 +151,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
       : "memory");
 }
 
+// TMA tiled 2-D store of one box from shared memory at (x, y), tracked by
+// the bulk-group of this thread.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tmap),
+      "r"(src), "r"(x), "r"(y)
+      : "memory");
+}
+
 // Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to
 // another CTA's, counted on that CTA's mbarrier (complete_tx).
 __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src_cta,
