@@ -244,8 +244,9 @@ int plan_max_range(int kind) {
 // range past a token's valid count yields an empty partial (0, -inf) that the
 // combine ignores.
 //  - kernel family: E4M3 caches with per-(slot, group) scales (every layout)
-//    and per-tensor E4M3 with h <= 16 run on the E4M3-operand keys-major
-//    kernel (one CTA per token, range and group of 16 heads); bf16 with
+//    and per-tensor E4M3 with h <= 64 run on the E4M3-operand keys-major
+//    kernel (one CTA per token, range and group of 16 heads; FP8 NoPE decode
+//    at h = 64: 0.079 ms there, 0.088 ms on the heads-major kernel); bf16 with
 //    h <= 16 on the bf16 keys-major kernel (one CTA per unit); bf16 and
 //    per-tensor E4M3 with more heads on the heads-major kernel (a 2-SM
 //    cluster per unit, up to 128 heads).
@@ -258,7 +259,7 @@ Plan make_plan(int T, int h, int d_qk, int d_v, int topk, int kv_format,
                int num_sms) {
   Plan pl{};
   int splits = 1, gran = 32;
-  const bool fp8 = tc_fp8_supported(h, d_qk, kv_format) && (kv_format != kE4m3 || h <= 16);
+  const bool fp8 = tc_fp8_supported(h, d_qk, kv_format) && (kv_format != kE4m3 || h <= 64);
   const bool keys = !fp8 && tc_keys_supported(h, d_qk, kv_format);
   if (fp8 || keys || tc_supported(h, d_qk, kv_format)) {
     pl.kind = fp8 ? kKernelTcFp8 : keys ? kKernelTcKeys : kKernelTc;

@@ -306,7 +306,7 @@ def test_full_config_sampled(cuda_lib, name, n_rand):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("kv_dtype,h,topk", [(0, 128, 2048), (1, 64, 2048), (0, 32, 4000)])
+@pytest.mark.parametrize("kv_dtype,h,topk", [(0, 128, 2048), (1, 96, 2048), (0, 32, 4000)])
 def test_longest_first_order_variable_units(cuda_lib, kv_dtype, h, topk):
     """More units than clusters, with valid counts that vary (0 .. topk):
     the heads-major kernel takes the units longest first, each CTA finding

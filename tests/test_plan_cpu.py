@@ -26,9 +26,9 @@ def plan(T, h, topk, kv=0, d_qk=576, sms=SMS):
 
 def family(h, kv):
     """E4M3 caches with group scales (every layout, any h) and per-tensor
-    E4M3 with h <= 16: the E4M3-operand keys-major kernel; bf16 with h <= 16:
+    E4M3 with h <= 64: the E4M3-operand keys-major kernel; bf16 with h <= 16:
     the bf16 keys-major kernel; the rest: the heads-major kernel."""
-    if kv in (2, 3, 4) or (kv == 1 and h <= 16):
+    if kv in (2, 3, 4) or (kv == 1 and h <= 64):
         return "tc_keys_fp8"
     return "tc_keys" if h <= 16 else "tc_heads"
 

@@ -31,7 +31,8 @@ def test_dispatch_uses_keys_kernels_up_to_16_heads(cuda_lib):
                 want = "tc_keys" if kv == 0 else "tc_keys_fp8"
                 assert info["kernel"] == want, (kv, h, d, info)
     assert cuda_lib.smla_plan_info(512, 17, 576, 2048, 0)["kernel"] == "tc_heads"
-    assert cuda_lib.smla_plan_info(512, 17, 576, 2048, 1)["kernel"] == "tc_heads"
+    assert cuda_lib.smla_plan_info(512, 64, 576, 2048, 1)["kernel"] == "tc_keys_fp8"
+    assert cuda_lib.smla_plan_info(512, 65, 576, 2048, 1)["kernel"] == "tc_heads"
     for kv in (2, 3, 4):
         assert cuda_lib.smla_plan_info(512, 128, 576, 2048, kv)["kernel"] == "tc_keys_fp8"
     assert cuda_lib.smla_plan_info(512, 16, 576, 4096, 2)["splits"] >= 2
