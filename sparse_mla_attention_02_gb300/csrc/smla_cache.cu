@@ -12,10 +12,16 @@
 //             saturating at +-448 (the satfinite conversion).
 // HBM-bound: per row 2 * d_qk bytes read, d_qk + 4 * G written.
 //
-// One warp per token row.  The row is 64 (d_qk 512) or 72 (576) chunks of
-// 8 channels; lane l converts chunks l, l + 32 and, for the rope group,
-// 64 + l (l < 8).  A group's chunks sit in one half-warp (16 lanes; the rope
-// group in 8), so the group max is a shuffle reduction within it.
+// Eight lanes per token row, four rows per warp.  A row is 64 (d_qk 512) or
+// 72 (576) chunks of 8 channels; lane j of the row's eight converts chunks
+// j + 8 i, i < 8 or 9 (all of its loads issued first), so that group g is
+// chunks i = 2g, 2g + 1 of all eight lanes (the rope group, i = 8, alone):
+// the group max is a shuffle reduction over the eight lanes.
+//
+// The kernel is bound by instruction issue as much as by HBM, so the fp32
+// quotients take no division: each is the IEEE quotient x / scale, reached
+// by one multiply and two fused multiply-adds (Markstein's correction of
+// x * RN(1/scale)), in packed f32x2 arithmetic.
 #include <cuda_bf16.h>
 
 #include "smla_internal.h"
@@ -31,7 +37,7 @@ struct CacheArgs {
   float* scales;          // [num_slots, G]
   int* status;
   int64_t num_slots;
-  int N, d_qk, G;
+  int N;
 };
 
 // Two floats -> two E4M3 codes (RN, saturating): lo in the low byte.
@@ -41,52 +47,169 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return r;
 }
 
-__global__ void __launch_bounds__(256) smla_cache_write_kernel(const CacheArgs a) {
-  const int lane = threadIdx.x & 31;
-  const int n = (int)((blockIdx.x * 256u + threadIdx.x) >> 5);
-  if (n >= a.N) return;
-  const int s = __ldg(a.slot + n);
-  if (s < 0) return;
-  if (s >= a.num_slots) {
-    if (lane == 0) atomicCAS(a.status, 0, kStatusBadIndex);
-    return;
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// RN(amax / 448) without a division: amax * RN(1/448) is within an ulp and
+// one fma residual correction (Markstein) rounds it; checked against the
+// IEEE quotient for every positive finite bf16 amax (amax is a bf16 value).
+__device__ __forceinline__ float amax_over_448(float amax) {
+  constexpr float kInv = 1.f / 448.f;
+  const float q0 = amax * kInv;
+  if (!(amax <= 3.0e38f)) return q0;                 // inf: inf / 448
+  return fmaf(fmaf(-q0, 448.f, amax), kInv, q0);
+}
+
+// RN(1/s) for a normal s: one Newton step from the hardware approximation
+// (within an ulp); checked for the scale of every bf16 amax mantissa, from
+// the approximation and from both of its fp32 neighbours.
+__device__ __forceinline__ float recip_rn(float s) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(s));
+  return fmaf(fmaf(-s, y, 1.f), y, y);
+}
+
+// Scales whose quotients the main path does not cover: below 2^-64 (the
+// residual could lose bits to underflow), inf and NaN.  The largest finite
+// scale (bf16 amax / 448) is below 2^120.
+__device__ __forceinline__ bool special_scale(float s) {
+  return !(s >= 0x1p-64f && s <= 0x1p120f);
+}
+
+// Quotients of 8 channels given as their negations xn (two per 64-bit word)
+// with ny = -RN(1/s):
+//   q0 = x * y,  u = q0 * s - x (exact, one fma),  q = q0 - u * y.
+// q is RN(x / s) (Markstein: y the correctly rounded reciprocal, q0 within
+// an ulp), checked for every bf16 x against every bf16 amax's scale.  The
+// negated inputs make the signs of zeros come out as the division's.
+__device__ __forceinline__ uint2 codes8(const uint64_t (&xn)[4], uint64_t s2, uint64_t ny2) {
+  uint32_t c[4];
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const uint64_t q0 = mul2(xn[p], ny2);
+    const uint64_t u = fma2(q0, s2, xn[p]);
+    float lo, hi;
+    unpack2(fma2(u, ny2, q0), lo, hi);
+    c[p] = e4m3x2(lo, hi);
   }
-  const int nchunks = a.d_qk / 8;
+  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
+// A 16-byte chunk of 8 bf16 -> their negations as 4 packed fp32 pairs, and
+// the largest magnitude folded into amax.
+__device__ __forceinline__ void unpack_neg8(const uint4 v, uint64_t (&xn)[4], float& amax) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int pass = 0; pass < 3; ++pass) {
-    const int k = 32 * pass + lane;                  // this lane's chunk
-    const bool live = pass < 2 ? k < nchunks : (nchunks > 64 && lane < 8);
-    // channels 8k..8k+7: kv_c for k < 64, k_pe after
-    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-    if (live)
-      raw = k < 64 ? __ldg(reinterpret_cast<const uint4*>(a.kv_c + (int64_t)n * 512) + k)
-                   : __ldg(reinterpret_cast<const uint4*>(a.k_pe + (int64_t)n * (a.d_qk - 512)) +
-                           (k - 64));
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-    float x[8];
+  for (int p = 0; p < 4; ++p) {
+    const float lo = __uint_as_float((w[p] << 16) ^ 0x80000000u);
+    const float hi = __uint_as_float((w[p] & 0xFFFF0000u) ^ 0x80000000u);
+    amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+    xn[p] = pack2(lo, hi);
+  }
+}
+
+// One chunk's codes for a special scale (the rare tail): a tiny scale and
+// the chunk are first multiplied by 2^64 (the quotients are unchanged); inf
+// and NaN scales give x * rcp(scale) (x / inf = +-0 for finite x, NaN for
+// x = inf; x / NaN = NaN).
+__device__ __forceinline__ uint2 special_codes8(const uint4 v, float s) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float q[8];
+  if (s < 0x1p-64f) {
+    const float ss = s * 0x1p64f;
+    const float y = recip_rn(ss);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      x[2 * e] = __uint_as_float(w[e] << 16);
-      x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t b = e & 1 ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16);
+      const float xn = -__uint_as_float(b) * 0x1p64f;
+      const float q0 = xn * -y;
+      q[e] = fmaf(fmaf(q0, ss, xn), -y, q0);
     }
+  } else {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t b = e & 1 ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16);
+      q[e] = __uint_as_float(b) * r;
+    }
+  }
+  return make_uint2(e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16),
+                    e4m3x2(q[4], q[5]) | (e4m3x2(q[6], q[7]) << 16));
+}
+
+// kChunks = d_qk / 64: 9 (kv_c + rope) or 8 (kv_c only).
+template <int kChunks>
+__global__ void __launch_bounds__(256) smla_cache_write_kernel(const CacheArgs a) {
+  constexpr int kD = 8 * 8 * kChunks;                // d_qk
+  constexpr int kG = (kChunks + 1) / 2;              // groups
+  const int j = threadIdx.x & 7;                     // lane within the row's eight
+  const int n = (int)((blockIdx.x * 256u + threadIdx.x) >> 3);
+  int s = n < a.N ? __ldg(a.slot + n) : -1;
+  if (s >= a.num_slots) {
+    if (j == 0) atomicCAS(a.status, 0, kStatusBadIndex);
+    s = -1;
+  }
+  const bool ok = s >= 0;
+  // chunk i of this lane: channel 8 (j + 8 i)
+  auto src = [&](int i) {
+    return i < 8 ? reinterpret_cast<const uint4*>(a.kv_c + (int64_t)n * 512) + j + 8 * i
+                 : reinterpret_cast<const uint4*>(a.k_pe + (int64_t)n * 64) + j;
+  };
+  uint4 raw[kChunks];
+#pragma unroll
+  for (int i = 0; i < kChunks; ++i) {
+    raw[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (ok) raw[i] = __ldg(src(i));
+  }
+  uint8_t* row = a.cache + (int64_t)s * kD;
+  float* srow = a.scales + (int64_t)s * kG;
+  uint32_t special = 0;                              // groups with a special scale
+  float scale_g[kG];
+#pragma unroll
+  for (int g = 0; g < kG; ++g) {
+    const int i0 = 2 * g, nc = (2 * g + 1 < kChunks) ? 2 : 1;
+    uint64_t xn[2][4];
     float amax = 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
-    // group max: within the half-warp (passes 0, 1) or lanes 0..7 (pass 2)
-    const int width = pass < 2 ? 16 : 8;
+    for (int c = 0; c < nc; ++c) unpack_neg8(raw[i0 + c], xn[c], amax);
 #pragma unroll
-    for (int o = 8; o >= 1; o >>= 1)
-      if (o < width) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    if (!live) continue;
-    const float scale = amax > 0.f ? amax / 448.f : 1.f;
-    const uint32_t c01 = e4m3x2(x[0] / scale, x[1] / scale);
-    const uint32_t c23 = e4m3x2(x[2] / scale, x[3] / scale);
-    const uint32_t c45 = e4m3x2(x[4] / scale, x[5] / scale);
-    const uint32_t c67 = e4m3x2(x[6] / scale, x[7] / scale);
-    *reinterpret_cast<uint2*>(a.cache + (int64_t)s * a.d_qk + 8 * k) =
-        make_uint2(c01 | (c23 << 16), c45 | (c67 << 16));
-    const int g = k >> 4;                            // 128-channel group
-    if ((k & 15) == 0) a.scales[(int64_t)s * a.G + g] = scale;
+    for (int o = 4; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float scale = amax > 0.f ? amax_over_448(amax) : 1.f;
+    scale_g[g] = scale;
+    special |= special_scale(scale) ? 1u << g : 0u;
+    const float ny = -recip_rn(scale);
+    const uint64_t s2 = pack2(scale, scale), ny2 = pack2(ny, ny);
+    if (ok) {
+#pragma unroll
+      for (int c = 0; c < nc; ++c)
+        *reinterpret_cast<uint2*>(row + 8 * (j + 8 * (i0 + c))) = codes8(xn[c], s2, ny2);
+      if (j == 0) srow[g] = scale;
+    }
+  }
+  if (ok && special) {                               // rare: redo the special groups
+#pragma unroll
+    for (int g = 0; g < kG; ++g) {
+      if (!(special >> g & 1u)) continue;
+      for (int i = 2 * g; i < 2 * g + 2 && i < kChunks; ++i)
+        *reinterpret_cast<uint2*>(row + 8 * (j + 8 * i)) = special_codes8(__ldg(src(i)), scale_g[g]);
+    }
   }
 }
 
@@ -104,10 +227,11 @@ cudaError_t launch_cache_write(const void* kv_c, const void* k_pe, const int32_t
   a.status = status;
   a.num_slots = num_slots;
   a.N = N;
-  a.d_qk = d_qk;
-  a.G = (d_qk + 127) / 128;
-  const unsigned blocks = (unsigned)(((int64_t)N * 32 + 255) / 256);
-  smla_cache_write_kernel<<<blocks, 256, 0, stream>>>(a);
+  const unsigned blocks = (unsigned)(((int64_t)N * 8 + 255) / 256);
+  if (d_qk == 576)
+    smla_cache_write_kernel<9><<<blocks, 256, 0, stream>>>(a);
+  else
+    smla_cache_write_kernel<8><<<blocks, 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

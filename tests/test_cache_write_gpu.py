@@ -102,3 +102,65 @@ def test_written_cache_feeds_the_forward(cuda_lib, h):
     inf = np.isneginf(Lr)
     assert np.array_equal(np.isneginf(Lg), inf)
     assert np.abs(Lg[~inf] - Lr[~inf]).max() <= 1e-3
+
+
+def _exhaustive_rows(d_qk):
+    """Groups whose first value is the group's amax and whose other values
+    run through every bf16 magnitude from amax down to amax * 2^-24 (both
+    signs), for each of the 128 bf16 mantissas of amax at several exponents,
+    plus groups with a tiny amax (a subnormal fp32 scale).  These hold every
+    quotient x / scale the normal range can give, the exact E4M3 rounding
+    ties (amax = 1.75 * 2^k makes the scale a power of two) and the quotients
+    within an ulp of a tie."""
+    vals = []
+    mant = np.arange(128, dtype=np.uint32)
+    rng = np.random.default_rng(5)
+    for i in range(128):
+        e = int(rng.integers(-30, 30))
+        amax_bits = np.uint32(((e + 127) << 7) | i)
+        xs = []
+        for de in range(0, 25):
+            eb = e + 127 - de
+            if eb < 1:
+                break
+            b = (np.uint32(eb) << 7) | mant
+            xs.append(b[b <= amax_bits])
+        xs = np.concatenate(xs).astype(np.uint16)
+        xs = np.concatenate([xs, xs | 0x8000])
+        for c in range(0, xs.size, 127):
+            vals.append(np.concatenate([[amax_bits], xs[c:c + 127]]).astype(np.uint16))
+    for amax_bits in (0x0001, 0x0003, 0x007F, 0x0080, 0x0105, 0x1A37):   # tiny and subnormal amax
+        xs = np.arange(1, amax_bits + 1, dtype=np.uint32)[:127].astype(np.uint16)
+        vals.append(np.concatenate([[amax_bits], xs]).astype(np.uint16))
+    groups = np.zeros((len(vals), 128), dtype=np.uint16)
+    for gi, v in enumerate(vals):
+        groups[gi, :v.size] = v
+    per_row = d_qk // 128
+    pad = (-len(groups)) % per_row
+    groups = np.concatenate([groups, np.zeros((pad, 128), dtype=np.uint16)])
+    return groups.reshape(-1, d_qk)
+
+
+def test_cache_write_is_exact_for_every_bf16_quotient(cuda_lib):
+    """Every E4M3 code equals the code of the IEEE fp32 quotient, over the
+    exhaustive quotient set of _exhaustive_rows (the fast kernel multiplies
+    by an approximate reciprocal and settles the few quotients near a
+    rounding midpoint with a residual test)."""
+    smla = cuda_lib
+    smla.smla_get_device_status(clear=True)
+    d_qk = 512
+    bits = _exhaustive_rows(d_qk)
+    N = bits.shape[0]
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    cache = torch.zeros((N, d_qk), dtype=torch.uint8, device="cuda")
+    scales = torch.zeros((N, 4), dtype=torch.float32, device="cuda")
+    smla.smla_cache_write_e4m3_group(x.cuda(), None, torch.arange(N, dtype=torch.int32, device="cuda"),
+                                     cache, scales)
+    torch.cuda.synchronize()
+    assert smla.smla_get_device_status(clear=True) == 0
+    ref_c = np.zeros((N, d_qk), dtype=np.uint8)
+    ref_s = np.zeros((N, 4), dtype=np.float32)
+    oracle.cache_write_e4m3_group(bits, None, np.arange(N, dtype=np.int32), ref_c, ref_s)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
+    got = cache.cpu().numpy()
+    assert np.array_equal(got, ref_c), f"{int((got != ref_c).sum())} codes differ"
