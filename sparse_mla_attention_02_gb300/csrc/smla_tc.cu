@@ -674,7 +674,8 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
       __syncwarp();
       tc_fence_after();
     }
-    const bool empty = !(l_tot > 0.f) || nb == 0;
+    // empty: no valid key (a NaN row sum, from a NaN in the cache, is not)
+    const bool empty = l_tot == 0.f || nb == 0;
     const float inv = empty ? 0.f : __fdividef(kscale, l_tot);   // (IEEE division: slow here)
     const bool live = head < p.h;          // pad rows past h are not written
     const int64_t orow = (int64_t)t * p.h + (live ? head : 0);

@@ -881,7 +881,7 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
       float inv[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i)   // (fast division: the IEEE one costs ~125 cycles each here)
-        inv[i] = l_tot[i] > 0.f ? __fdividef(oscale, l_tot[i] * kPShift) : 0.f;
+        inv[i] = l_tot[i] != 0.f ? __fdividef(oscale, l_tot[i] * kPShift) : 0.f;
       // bf16 O goes through the staging rows [16 heads][512] and leaves as
       // one bulk copy (the token's rows of these heads are contiguous); the
       // previous unit's copy has read the staging rows before they are
@@ -906,7 +906,7 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
         for (int i = 0; i < 8; ++i) {
           // (no valid key for the head, or none with a nonzero scale in this
           // group: 0 exactly)
-          const float o = (inv[i] > 0.f && rinv > 0.f)
+          const float o = (l_tot[i] != 0.f && rinv > 0.f)
                               ? fmaf(__uint_as_float(wl8[i]), 0.0625f, __uint_as_float(wh[i])) *
                                     (inv[i] * rinv)
                               : 0.f;
@@ -939,7 +939,7 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
           mi = key == i ? m_run[i] : mi;
           li = key == i ? l_tot[i] : li;
         }
-        const bool empty = !(li > 0.f);
+        const bool empty = li == 0.f;         // (a NaN row sum is not empty)
         const float lse_v = empty ? -INFINITY : (mi + log2f(li)) * 0.69314718055994530942f;
         const int64_t orow = (int64_t)ui.t * p.h + ui.h0 + 8 * wg + key;
         if (p.fp32_out)

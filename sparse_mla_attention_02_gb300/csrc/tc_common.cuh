@@ -82,15 +82,16 @@ __device__ __forceinline__ Waiter make_waiter(volatile int* abort_flag, const Fw
 // is a bf16 value.  The byte's exponent and mantissa fields are placed in the
 // bf16 fields (which reads the value times 2^-120, bias 7 vs 127; E4M3
 // subnormals land on bf16 subnormals), then one exact bf16 multiply by 2^120
-// restores it.  The E4M3 NaN code is not special-cased (the generator never
-// writes it).
+// restores it.  The NaN codes S.1111.111 (which the placement would read as
+// +-480) are made bf16 NaN, as the format defines them.
 __device__ __forceinline__ uint32_t e4m3x2_lanes_to_bf16x2(uint32_t x) {
   // x holds one byte in the low byte of each 16-bit lane
   uint32_t bits = ((x & 0x007F007Fu) << 4) | ((x & 0x00800080u) << 8);
   __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&bits);
   const uint32_t k2 = 0x7B807B80u;                 // (2^120, 2^120) in bf16
   v = __hmul2(v, *reinterpret_cast<const __nv_bfloat162*>(&k2));
-  return *reinterpret_cast<uint32_t*>(&v);
+  const uint32_t nan = __vcmpeq2(x & 0x007F007Fu, 0x007F007Fu);   // 0xFFFF per NaN code
+  return *reinterpret_cast<uint32_t*>(&v) | (nan & 0x7FC07FC0u);
 }
 __device__ __forceinline__ void e4m3x4_to_bf16(uint32_t w, uint32_t& lo, uint32_t& hi) {
   lo = e4m3x2_lanes_to_bf16x2(__byte_perm(w, 0u, 0x4140u));   // bytes 0, 1

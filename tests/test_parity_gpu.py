@@ -333,3 +333,34 @@ def test_longest_first_order_variable_units(cuda_lib, kv_dtype, h, topk):
     sel = sorted(set(range(0, T, 7)) | {0, 1, 2, T - 1})
     Or, Lr = oracle_fwd(w, tokens=sel)
     compare(out[sel], lse[sel], Or, Lr, w.name)
+
+
+@pytest.mark.parametrize("kv_dtype,h", [(1, 16), (1, 128), (2, 16), (2, 64), (3, 64)])
+def test_e4m3_nan_codes_propagate(cuda_lib, kv_dtype, h):
+    """The E4M3 codes S.1111.111 (0x7F, 0xFF) are NaN in the format (the
+    float8_e4m3fn the pages name).  A NaN code in a row that a token selects
+    makes that token's scores, LSE and output NaN, as the oracle gives; the
+    same code in a row that only sits past another token's valid count
+    changes nothing there.  Every kernel family that reads E4M3 caches
+    (E4M3-operand keys-major, heads-major with its bf16 converter) agrees."""
+    T = 3
+    w = W.custom(T=T, h=h, topk=64, num_slots=200, kv_dtype=kv_dtype,
+                 valid=[64, 20, 33], seed=880 + kv_dtype + h)
+    row_sel = int(w.indices[0, 5])            # selected by token 0
+    w.kv[row_sel, 7] = 0x7F
+    # a row no token selects within its valid count, whose id is placed past
+    # token 1's valid count (an entry there is ignored)
+    valid_rows = set(w.indices[0].tolist()) | set(w.indices[1, :20].tolist()) | \
+        set(w.indices[2, :33].tolist())
+    row_past = min(set(range(200)) - valid_rows)
+    w.kv[row_past, 300] = 0xFF
+    w.indices[1, 40] = row_past
+    wd = w.to("cuda")
+    O, L = gpu_fwd(cuda_lib, wd)
+    Or, Lr = oracle_fwd(w)
+    assert np.isnan(Lr[0]).all() and np.isnan(Or[0]).all()      # the oracle's reading
+    assert torch.isnan(L[0]).all() and torch.isnan(O[0].float()).all()
+    for t in (1, 2):
+        if row_sel in set(w.indices[t, :int(w.valid_len[t])].tolist()):
+            continue                          # (the random rows may share the NaN row)
+        compare(O[t:t + 1], L[t:t + 1], Or[t:t + 1], Lr[t:t + 1], f"nan_codes t={t}")
