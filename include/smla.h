@@ -139,7 +139,8 @@ SMLA_API size_t smla_workspace_size(int T, int h, int d_qk, int d_v, int topk,
 
 /* Kernel families a plan can choose (see smla_plan_info). */
 typedef enum {
-  SMLA_KERNEL_CUDA_CORE = 0,     /* fp32 CUDA-core kernel (any supported shape) */
+  SMLA_KERNEL_CUDA_CORE = 0,     /* (not chosen by any plan: every supported shape has a
+                                    tensor-core kernel; the value stays reserved) */
   SMLA_KERNEL_TC_HEADS = 1,      /* tcgen05, heads as the MMA rows (h <= 128) */
   SMLA_KERNEL_TC_KEYS = 2,       /* tcgen05, top-k positions as the MMA rows (bf16, h <= 16) */
   SMLA_KERNEL_TC_KEYS_FP8 = 3    /* tcgen05 with E4M3 operands, top-k positions as the MMA

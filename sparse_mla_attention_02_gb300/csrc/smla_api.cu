@@ -129,12 +129,12 @@ smla_status run_fwd(const void* q, const void* kv, int kv_dtype,
   }
   smla::Plan plan =
       smla::make_plan(T, h, d_qk, d_v, topk, kv_dtype, dev->num_sms);
+  if (plan.kind == smla::kKernelNone) return SMLA_ERR_UNSUPPORTED;
   if (out_f32) {
     // Partial-output mode: one range per token, written straight to the
     // caller's fp32 buffers (no workspace, no combine).  A top-k longer than
     // one range of the chosen kernel would need a split: not served.
-    if (plan.kind != smla::kKernelSimt && topk > smla::plan_max_range(plan.kind))
-      return SMLA_ERR_UNSUPPORTED;
+    if (topk > smla::plan_max_range(plan.kind)) return SMLA_ERR_UNSUPPORTED;
     plan.splits = 1;
     plan.split_len = topk;
     plan.workspace_bytes = 0;
@@ -207,8 +207,7 @@ smla_status run_fwd(const void* q, const void* kv, int kv_dtype,
   }
   const cudaError_t le = plan.kind == smla::kKernelTcFp8    ? smla::launch_tc_fp8(p, stream)
                          : plan.kind == smla::kKernelTcKeys ? smla::launch_tc_keys(p, stream)
-                         : plan.kind == smla::kKernelTc     ? smla::launch_tc(p, stream)
-                                                            : smla::launch_simt(p, stream);
+                                                            : smla::launch_tc(p, stream);
   if (le != cudaSuccess) return SMLA_ERR_CUDA;
   if (plan.splits > 1) {
     if (smla::launch_combine(p.o_part, p.lse_part, plan.splits, (int64_t)T * h,
@@ -253,15 +252,17 @@ int plan_max_range(int kind) {
 //  - tensor-core paths: split only when the units alone leave more than half
 //    of the SMs (or SM pairs) idle (each split costs partial-O traffic), or
 //    when topk is longer than one unit's range.
-//  - CUDA-core path: enough (token, 16-head group, range) units to fill every
-//    SM twice.
 Plan make_plan(int T, int h, int d_qk, int d_v, int topk, int kv_format,
                int num_sms) {
   Plan pl{};
-  int splits = 1, gran = 32;
+  int splits = 1, gran = 64;
   const bool fp8 = tc_fp8_supported(h, d_qk, kv_format) && (kv_format != kE4m3 || h <= 64);
   const bool keys = !fp8 && tc_keys_supported(h, d_qk, kv_format);
-  if (fp8 || keys || tc_supported(h, d_qk, kv_format)) {
+  if (!fp8 && !keys && !tc_supported(h, d_qk, kv_format)) {
+    pl.kind = kKernelNone;              // (argument checks reject such shapes first)
+    return pl;
+  }
+  {
     pl.kind = fp8 ? kKernelTcFp8 : keys ? kKernelTcKeys : kKernelTc;
     gran = fp8 ? 128 : 64;
     const int max_range = plan_max_range(pl.kind);
@@ -278,18 +279,6 @@ Plan make_plan(int T, int h, int d_qk, int d_v, int topk, int kv_format,
     }
     const int need = (topk + max_range - 1) / max_range;
     if (splits < need) splits = need;
-  } else {
-    pl.kind = kKernelSimt;
-    const int64_t groups = (h + 15) / 16;
-    const int64_t units = (int64_t)T * groups;
-    const int64_t want = 2LL * (num_sms > 0 ? num_sms : 1);
-    if (units < want) {
-      splits = (int)((want + units - 1) / units);
-      const int max_by_topk = (topk + 127) / 128;
-      if (splits > max_by_topk) splits = max_by_topk;
-      if (splits > 64) splits = 64;
-      if (splits < 1) splits = 1;
-    }
   }
   int len = (topk + splits - 1) / splits;
   len = (len + gran - 1) / gran * gran;
@@ -433,8 +422,7 @@ smla_status smla_plan_info_for(int T, int h, int d_qk, int d_v, int topk,
   if (kernel)
     *kernel = pl.kind == smla::kKernelTcFp8    ? SMLA_KERNEL_TC_KEYS_FP8
               : pl.kind == smla::kKernelTcKeys ? SMLA_KERNEL_TC_KEYS
-              : pl.kind == smla::kKernelTc     ? SMLA_KERNEL_TC_HEADS
-                                               : SMLA_KERNEL_CUDA_CORE;
+                                               : SMLA_KERNEL_TC_HEADS;
   if (splits) *splits = pl.splits;
   if (workspace_bytes) *workspace_bytes = pl.workspace_bytes;
   return SMLA_OK;

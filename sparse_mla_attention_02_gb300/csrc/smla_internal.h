@@ -107,7 +107,7 @@ __device__ __forceinline__ int token_req(const FwdParams& p, int t, bool& bad) {
 #endif
 
 // Which kernel family a plan uses.
-enum KernelKind { kKernelSimt = 0, kKernelTc = 1, kKernelTcKeys = 2, kKernelTcFp8 = 3 };
+enum KernelKind { kKernelNone = 0, kKernelTc = 1, kKernelTcKeys = 2, kKernelTcFp8 = 3 };
 
 struct Plan {
   int kind;
@@ -132,7 +132,6 @@ int check_fwd_args_code(const void* q, const void* kv, int kv_dtype, const float
 Plan make_plan(int T, int h, int d_qk, int d_v, int topk, int kv_format,
                int num_sms);
 
-cudaError_t launch_simt(const FwdParams& p, cudaStream_t stream);
 bool tc_supported(int h, int d_qk, int kv_format);
 int tc_max_range();  // largest top-k range one tensor-core unit covers
 cudaError_t launch_tc(const FwdParams& p, cudaStream_t stream);

@@ -1,6 +1,6 @@
 // smla_tc_keys.cu — tensor-core (tcgen05 / TMEM) sparse MLA forward for up
-// to 16 heads, every cache format, including E4M3 with one scale per
-// (slot, 128-channel group).
+// to 16 heads with a bf16 cache.  (E4M3 caches run on the E4M3-operand
+// kernel of smla_tc_fp8.cu.)
 //
 // With few heads, the heads cannot fill a 128-row MMA, so this kernel turns
 // both products around: the top-k positions (keys) of a block are the MMA's
@@ -16,16 +16,9 @@
 // columns of its own half, key r % 64's partial scores over half h (the
 // other 16 columns pair a key half with the other Q half and are ignored).
 // The two halves of a key are summed through shared memory by the two
-// threads that own them; no score crosses an SM.
-//   * Group scales: one fp32 QK accumulator per channel group of a half
-//     (two ckv groups and the rope), so a key's group scale multiplies its
-//     partial score exactly (in fp32) before the groups are summed.
-//   * PV: O^T is four 128-channel blocks (one per ckv group); block c reads
-//     V^T from tile rows [64 (c / 2), 64 (c / 2) + 64).  With group scales,
-//     P^T is stored once per group, each key's entry multiplied by that
-//     key's group scale, as a bf16 pair hi + lo side by side in N (N = 32),
-//     summed in the epilogue, so O keeps the exact scale; a single bf16
-//     rounding of p * scale would put up to 2^-9 relative error on O.
+// threads that own them; no score crosses an SM.  PV: O^T is four
+// 128-channel blocks; block c reads V^T from tile rows [64 (c / 2),
+// 64 (c / 2) + 64).
 // Thread t of the softmax warpgroup owns tile row t (TMEM lane t): key
 // t % 64 and heads [8 (t / 64), 8 (t / 64) + 8).  The per-head max over the
 // block's keys is reduced only when some score passes the running max by
@@ -34,26 +27,21 @@
 //
 // Method steps (vLLM "Sparse MLA on Hopper" diff, ops/cutlass_fa3.py docstring:
 // score = q_rope.k_rope + q_nope.c_kv, output = softmax(score*scale) @ c_kv;
-// flashinfer_mla_sparse_sm90.py, module docstring: FP8 cache read directly
-// with a per-tensor k_scale or per-token x 128-channel-group scales;
-// forward_mqa: compacted valid prefix with -1 past it; vLLM API docs
-// flashmla_sparse, _forward_fp8_kv_mixed_batch: empty rows give (O = 0,
-// LSE = -inf)):
+// flashinfer_mla_sparse_sm90.py, forward_mqa: compacted valid prefix with -1
+// past it; vLLM API docs flashmla_sparse, _forward_fp8_kv_mixed_batch: empty
+// rows give (O = 0, LSE = -inf)):
 //   a1 work setup: v = min(valid_len[t], topk); range [k0, k1) of the split
-//   a2 gather: slot ids -> 128-byte-swizzled bf16 tiles (TMA tile::gather4
-//      for bf16; E4M3 rows converted exactly on load); masked keys are zero
-//   a3 scales: per-tensor scale folded into the score scale and the output;
-//      group scales applied per group accumulator (QK) and per copy of P (PV)
+//   a2 gather: slot ids -> 128-byte-swizzled bf16 tiles (TMA tile::gather4);
+//      masked keys are zero
 //   a4 QK^T, a5 masked online softmax, a6 PV, a7 O / l and LSE = m + ln l
 //
 // Warp roles (320 threads): warp 0 issues the QK MMAs and owns TMEM; warp 9
-// issues the PV MMAs; warps 1..4 load the unit's slot ids, then gather
-// (bf16: TMA; E4M3: each warp loads 32 tile rows cooperatively, 16 lanes a
-// row, and converts and stores what it loaded); warps 5..8 (thread <-> tile
-// row <-> TMEM lane) load Q, combine the halves, run the softmax, the O
-// rescale and the epilogue.
+// issues the PV MMAs; warps 1..4 load the unit's slot ids, then gather with
+// TMA; warps 5..8 (thread <-> tile row <-> TMEM lane) load Q, combine the
+// halves, run the softmax, the O rescale and the epilogue.
 // Every wait is bounded; a wait that runs out records a timeout status, sets
-// an abort flag that skips later waits, and the block finishes normally.
+// an abort flag that skips later waits, and the block drains its copies and
+// MMAs and finishes normally.
 #include <math.h>
 
 #include "smla_internal.h"
@@ -73,7 +61,6 @@ constexpr int kStages = 2;                 // gathered-tile pipeline depth
 constexpr int kChunkBytes = kRows * 128;   // 64 channels x 128 rows, bf16
 constexpr int kMaxChunks = 5;              // 256 ckv + the rope chunk per row
 constexpr int kStageBytes = kMaxChunks * kChunkBytes;
-constexpr int kScaleBytes = kRows * 16;    // a row's group scales (3 + pad)
 constexpr int kQChunkBytes = kNq * 128;    // 64 channels x 32 Q rows
 constexpr int kPPlaneBytes = kBK * 128;    // P^T: 64 keys x 128 bytes
 constexpr int kPAreaBytes = 2 * kPPlaneBytes;
@@ -84,16 +71,14 @@ constexpr int kSoftmax = 128;              // warps 5..8
 constexpr int kMaxBlocks = 32;             // ranges up to 2048 positions
 
 // TMEM columns.
-constexpr uint32_t kColO = 0;              // O^T: 4 blocks of 128 channels x 32
-                                           // (16 heads, or hi | lo with group scales)
-constexpr uint32_t kColS = 128;            // S: 2 buffers x 3 accumulators x 32
-constexpr uint32_t kSBuf = 3 * kNq;
+constexpr uint32_t kColO = 0;              // O^T: 4 blocks of 128 channels x 32 (16 used)
+constexpr uint32_t kColS = 128;            // S: 2 buffers x 32
+constexpr uint32_t kSBuf = kNq;
 constexpr uint32_t kTmemCols = 512;
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
 constexpr uint32_t kOffTile = 0;
-constexpr uint32_t kOffScale = kOffTile + kStages * kStageBytes;
-constexpr uint32_t kOffQ = kOffScale + kStages * kScaleBytes;
+constexpr uint32_t kOffQ = kOffTile + kStages * kStageBytes;
 constexpr uint32_t kOffP = kOffQ + kMaxChunks * kQChunkBytes;      // P^T
 constexpr uint32_t kOffComb = kOffP + kPAreaBytes;                 // [2][128 rows][8] f32
 constexpr uint32_t kOffSlot = kOffComb + 2 * kCombBytes;           // [blocks*64] i32
@@ -106,8 +91,8 @@ enum {
   kBarKvEmpty = kBarKvFull + 2,     // [2]
   kBarSFull = kBarKvEmpty + 2,      // [2]
   kBarSEmpty = kBarSFull + 2,       // [2]
-  kBarPFull = kBarSEmpty + 2,       // [P buffers]
-  kBarPEmpty = kBarPFull + 2,       // [P buffers]
+  kBarPFull = kBarSEmpty + 2,       // [2 P buffers]
+  kBarPEmpty = kBarPFull + 2,       // [2 P buffers]
   kBarODone = kBarPEmpty + 2,
   kBarOFinal,                       // one phase: the unit's last PV is done
   kBarQReady,
@@ -123,10 +108,9 @@ static_assert(kOffComb % 16 == 0 && kOffBar % 8 == 0, "alignment");
 static_assert(kColS + 2 * kSBuf <= kTmemCols, "TMEM budget");
 
 struct KeysArgs {
-  CUtensorMap kv_map;  // bf16 cache as a 2-D tensor, 64-channel boxes (bf16 only)
+  CUtensorMap kv_map;  // bf16 cache as a 2-D tensor, 64-channel boxes
   FwdParams p;
   int ksteps;          // 16-channel QK steps per half row: 18 (d_qk 576) or 16 (512)
-  int G;               // scale groups per slot (group format)
   float scale_log2;    // sm_scale * log2(e)
 };
 
@@ -158,16 +142,11 @@ __device__ __forceinline__ float xreduce8(float (&v)[8], int lane) {
 
 // kLpt: the units are taken longest first (lpt_unit); a separate instance,
 // so that launches in unit order carry none of its code.
-template <int kFmt, bool kLpt>
+template <bool kLpt>
 __global__ void __launch_bounds__(kThreads, 1)
 smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
-  // Formats with per-(slot, group) scales: one QK accumulator per group.
-  constexpr bool kGroup = kFmt == kE4m3Group || kFmt == kDsMla || kFmt == kE4m3Group4Kpe;
-  constexpr bool kFp8 = kFmt != kBf16;
-  // P^T: with group scales one buffer of two planes (4 groups x hi | lo);
-  // otherwise one plane per buffer, double-buffered.
-  constexpr int kPBufs = kGroup ? 1 : 2;
-  constexpr int kNpv = kGroup ? 2 * kN : kN;                              // PV MMA N
+  constexpr int kPBufs = 2;                 // P^T double-buffered
+  constexpr int kNpv = kN;                  // PV MMA N
   extern __shared__ uint8_t smem_raw[];
   const FwdParams& p = a.p;
   const uint32_t raw = smem_u32(smem_raw);
@@ -191,7 +170,6 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
   // Local channels of a half row: steps 0..15 = ckv [256h, 256h + 256);
   // steps 16, 17 (d_qk 576) = rope [512 + 32h, 544 + 32h), held in chunk 4.
   const int ksteps = a.ksteps;
-  const int n_lg = kGroup ? (ksteps + 7) / 8 : 1;       // group accumulators
 
   auto bar = [&](int i) { return sb + kOffBar + 8u * (uint32_t)i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffAbort);
@@ -199,11 +177,10 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      // bf16: one expect_tx per TMA warp; E4M3: one arrival per loader thread
-      mbar_init(bar(kBarKvFull + s), kFp8 ? kProducers : 4);
+      mbar_init(bar(kBarKvFull + s), 4);           // one expect_tx per TMA warp
       mbar_init(bar(kBarKvEmpty + s), 1);
     }
-    for (int i = 0; i < 2; ++i) {     // (group scales use P barrier 0 only)
+    for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarSFull + i), 1);
       mbar_init(bar(kBarSEmpty + i), kSoftmax);
       mbar_init(bar(kBarPFull + i), kSoftmax);
@@ -281,9 +258,7 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
               if (ks < ksteps) {
                 const uint32_t oa = (uint32_t)((ks >> 2) * kChunkBytes + (ks & 3) * 32);
                 const uint32_t ob = (uint32_t)((ks >> 2) * kQChunkBytes + (ks & 3) * 32);
-                const uint32_t acc = kGroup ? (uint32_t)(ks >> 3) * kNq : 0u;
-                const bool first = kGroup ? (ks & 7) == 0 : ks == 0;
-                mma_ss(dS + acc, a0 + (oa >> 4), b0 + (ob >> 4), id_qk, first ? 0u : 1u);
+                mma_ss(dS, a0 + (oa >> 4), b0 + (ob >> 4), id_qk, ks == 0 ? 0u : 1u);
               }
             }
             mma_commit(bar(kBarSFull + s));
@@ -303,8 +278,7 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
             fence_proxy_async_smem();
             // A = V^T of channel block c: 128 channels (two 64-channel
             // chunks) x 16 keys, MN-major, from tile rows [64 (c / 2), +64);
-            // B = P^T: 16 keys x N, MN-major (group scales: plane c / 2,
-            // 64 (c % 2) bytes into each key's row).
+            // B = P^T: 16 keys x N, MN-major.
             const uint64_t a0 = sdesc(tile, kChunkBytes, 1024, kLayoutSw128);
             const uint64_t b0 = sdesc(pb, kPAreaBytes, 1024, kLayoutSw128);
             const uint32_t acc0 = j > 0 ? 1u : 0u;
@@ -314,9 +288,7 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
               for (int ks = 0; ks < kBK / 16; ++ks) {
                 const uint32_t oa =
                     (uint32_t)(2 * (c & 1) * kChunkBytes + (64 * (c >> 1) + 16 * ks) * 128);
-                const uint32_t ob =
-                    kGroup ? (uint32_t)((c >> 1) * kPPlaneBytes + 64 * (c & 1) + ks * 2048)
-                           : (uint32_t)(ks * 2048);
+                const uint32_t ob = (uint32_t)(ks * 2048);
                 mma_ss(tmem + kColO + 32u * (uint32_t)c, a0 + (oa >> 4), b0 + (ob >> 4), id_pv,
                        ks > 0 ? 1u : acc0);
               }
@@ -346,118 +318,7 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
     const int kb0 = w0 & (kBK - 1);                       // and its first key
     const int g_lo = 256 * half;                          // first ckv channel of the half
     const int rope_lo = 512 + 32 * half;                  // first rope channel of the half
-    if (kFp8) {
-      // Warp-cooperative gather: a row's 256 ckv bytes are read by 16 lanes,
-      // 16 bytes each, two rows per load instruction, so one instruction
-      // touches a few cache lines rather than 32; the rope pieces follow, 16
-      // (E4M3) or 8 (bf16) rows per instruction.  All loads of a block are in
-      // flight before the stage is awaited; then each lane converts what it
-      // loaded (exact E4M3 -> bf16) into the 128-byte-swizzled tile.  Masked
-      // rows are zero.  656-byte rows: the rope is bf16 (copied as it is),
-      // the group scales sit in the row, and the rope group's scale is 1.
-      const int hl = lane >> 4, pc = lane & 15;            // ckv: row of the pair, piece
-      const bool rope = ksteps > 16;                       // d_qk 576
-      constexpr int kRopeLanes = kFmt == kDsMla ? 4 : 2;   // 16-byte rope pieces a row
-      constexpr int kRopeRows = 32 / kRopeLanes;           // rows per rope instruction
-      constexpr int kRopeIns = 32 / kRopeRows;             // rope instructions per block
-      const int rpc = lane % kRopeLanes, rrow = lane / kRopeLanes;
-      const int row_bytes = kFmt == kDsMla ? kDsMlaRowBytes : p.d_qk;
-      const uint32_t rope_off =
-          kFmt == kDsMla ? (uint32_t)(kDsMlaRopeOff + 64 * half) : (uint32_t)rope_lo;
-      const int scale_stride = kFmt == kE4m3Group4Kpe ? 4 : a.G;
-      const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
-      const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
-      for (int b = 0; b < nb; ++b) {
-        const int s = b & 1;
-        const int* bs = slots + b * kBK + kb0;
-        uint4 ck[16], rq[kRopeIns];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int id = bs[2 * i + hl];
-          ck[i] = id >= 0 ? __ldg(reinterpret_cast<const uint4*>(
-                                      kv8 + (size_t)id * row_bytes + g_lo) + pc)
-                          : zero4;
-        }
-#pragma unroll
-        for (int j = 0; j < kRopeIns; ++j) {
-          const int id = bs[kRopeRows * j + rrow];
-          rq[j] = (rope && id >= 0) ? __ldg(reinterpret_cast<const uint4*>(
-                                                kv8 + (size_t)id * row_bytes + rope_off) + rpc)
-                                    : zero4;
-        }
-        // The lane's own row (w0 + lane): its group scales, and the row of
-        // the next block into L2 while this one is converted.
-        const int id = bs[lane];
-        const uint8_t* rowp = kv8 + (size_t)(id < 0 ? 0 : id) * row_bytes;
-        if (b + 1 < nb) {
-          const int idn = slots[(b + 1) * kBK + kb0 + lane];
-          if (idn >= 0) {
-            const uint8_t* rn = kv8 + (size_t)idn * row_bytes;
-            prefetch_l2(rn + g_lo);
-            prefetch_l2(rn + g_lo + 128);
-            prefetch_l2(rn + g_lo + 255);
-            if (rope) prefetch_l2(rn + rope_off);
-            if (kFmt == kDsMla) {
-              prefetch_l2(rn + kDsMlaScaleOff);
-              prefetch_l2(rn + rope_off + 63);
-            } else if (kGroup) {
-              prefetch_l2(p.k_scale + (int64_t)idn * scale_stride);
-            }
-          }
-        }
-        float sc[3] = {0.f, 0.f, 0.f};
-        if (kGroup && id >= 0) {
-          const float* srow = kFmt == kDsMla
-                                  ? reinterpret_cast<const float*>(rowp + kDsMlaScaleOff)
-                                  : p.k_scale + (int64_t)id * scale_stride;
-          sc[0] = __ldg(srow + 2 * half);
-          sc[1] = __ldg(srow + 2 * half + 1);
-          if (n_lg > 2)
-            sc[2] = kFmt == kE4m3Group ? __ldg(srow + 4) : kFmt == kDsMla ? 1.f : p.kpe_scale;
-        }
-        if (b >= kStages) W.wait(bar(kBarKvEmpty + s), ((b >> 1) - 1) & 1);
-        if (*abort_flag) break;                  // the stage may still be in use
-        uint8_t* tile = sm + kOffTile + s * kStageBytes;
-        // 16-byte unit cj (8 bf16 channels) of tile row `row`
-        auto unit = [&](int row, uint32_t cj) -> uint4* {
-          return reinterpret_cast<uint4*>(tile + row * 128 + (cj >> 3) * kChunkBytes +
-                                          (((cj & 7u) ^ ((uint32_t)row & 7u)) << 4));
-        };
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int row = w0 + 2 * i + hl;
-          uint32_t o[8];
-          e4m3x4_to_bf16_sx(ck[i].x, o[0], o[1]);
-          e4m3x4_to_bf16_sx(ck[i].y, o[2], o[3]);
-          e4m3x4_to_bf16_sx(ck[i].z, o[4], o[5]);
-          e4m3x4_to_bf16_sx(ck[i].w, o[6], o[7]);
-          *unit(row, 2u * (uint32_t)pc) = make_uint4(o[0], o[1], o[2], o[3]);
-          *unit(row, 2u * (uint32_t)pc + 1u) = make_uint4(o[4], o[5], o[6], o[7]);
-        }
-        if (rope) {
-#pragma unroll
-          for (int j = 0; j < kRopeIns; ++j) {
-            const int row = w0 + kRopeRows * j + rrow;
-            if (kFmt == kDsMla) {
-              *unit(row, 32u + (uint32_t)rpc) = rq[j];       // bf16, as is
-            } else {
-              uint32_t o[8];
-              e4m3x4_to_bf16_sx(rq[j].x, o[0], o[1]);
-              e4m3x4_to_bf16_sx(rq[j].y, o[2], o[3]);
-              e4m3x4_to_bf16_sx(rq[j].z, o[4], o[5]);
-              e4m3x4_to_bf16_sx(rq[j].w, o[6], o[7]);
-              *unit(row, 32u + 2u * (uint32_t)rpc) = make_uint4(o[0], o[1], o[2], o[3]);
-              *unit(row, 33u + 2u * (uint32_t)rpc) = make_uint4(o[4], o[5], o[6], o[7]);
-            }
-          }
-        }
-        if (kGroup)
-          *reinterpret_cast<float4*>(sm + kOffScale + s * kScaleBytes + (w0 + lane) * 16) =
-              make_float4(sc[0], sc[1], sc[2], 0.f);
-        fence_proxy_async_smem();
-        mbar_arrive(bar(kBarKvFull + s));
-      }
-    } else {
+    {
       // bf16: warp wl issues the 8 four-row groups of its 32 tile rows.
       const int n_boxes = ksteps > 16 ? 5 : 4;               // + one rope box
       const uint32_t tx_bytes = (uint32_t)(8 * n_boxes * 512);
@@ -527,9 +388,7 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
       fence_proxy_async_smem();
       mbar_arrive(bar(kBarQReady));
     }
-    // Per-tensor E4M3: the scale multiplies every score and output.
-    const float kscale = kFmt == kE4m3 ? __ldg(p.k_scale) : 1.f;
-    const float scale_log2 = a.scale_log2 * kscale;
+    const float scale_log2 = a.scale_log2;
     float m_run[8], l_part[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) { m_run[i] = -INFINITY; l_part[i] = 0.f; }
@@ -543,8 +402,6 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
     for (int b = 0; b < nb; ++b) {
       const int s = b & 1;
       float part[16];                      // this half's partial scores, heads 0..15
-      float scp[4] = {1.f, 1.f, 1.f, 1.f}; // the key's PV group scales (groups 0..3)
-      if (kGroup) W.wait(bar(kBarKvFull + s), (b >> 1) & 1);   // scale rows visible
       W.wait(bar(kBarSFull + s), (b >> 1) & 1);
       __syncwarp();
       tc_fence_after();
@@ -553,35 +410,10 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
         // with the Q rows of the same half.
         const uint32_t sc0 = tmem + lane_base + kColS + kSBuf * s + 16u * (uint32_t)hf;
         uint32_t w[16];
-        if (kGroup) {
-          const float4 sc =
-              *reinterpret_cast<const float4*>(sm + kOffScale + s * kScaleBytes + row * 16);
-          const float4 so =
-              *reinterpret_cast<const float4*>(sm + kOffScale + s * kScaleBytes + partner * 16);
-          scp[0] = hf ? so.x : sc.x;
-          scp[1] = hf ? so.y : sc.y;
-          scp[2] = hf ? sc.x : so.x;
-          scp[3] = hf ? sc.y : so.y;
-          // The group accumulators' loads are issued together, then awaited.
-          uint32_t w1[16], w2[16];
-          tmem_ld16(sc0, w);
-          tmem_ld16(sc0 + kNq, w1);
-          if (n_lg > 2) tmem_ld16(sc0 + 2 * kNq, w2);   // same for every lane
-          tmem_wait_ld();
+        tmem_ld16(sc0, w);
+        tmem_wait_ld();
 #pragma unroll
-          for (int hd = 0; hd < kN; ++hd)
-            part[hd] = fmaf(sc.y, __uint_as_float(w1[hd]), sc.x * __uint_as_float(w[hd]));
-          if (n_lg > 2) {
-#pragma unroll
-            for (int hd = 0; hd < kN; ++hd)
-              part[hd] = fmaf(sc.z, __uint_as_float(w2[hd]), part[hd]);
-          }
-        } else {
-          tmem_ld16(sc0, w);
-          tmem_wait_ld();
-#pragma unroll
-          for (int hd = 0; hd < kN; ++hd) part[hd] = __uint_as_float(w[hd]);
-        }
+        for (int hd = 0; hd < kN; ++hd) part[hd] = __uint_as_float(w[hd]);
       }
       tc_fence_before();
       mbar_arrive(bar(kBarSEmpty + s));
@@ -649,31 +481,10 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
         pe[i] = m_run[i] == -INFINITY ? 0.f : ex2_approx(sp[i] - m_run[i]);
         l_part[i] = fmaf(l_part[i], alpha[i], pe[i]);
       }
-      // a6 operand: P^T into buffer b % kPBufs (group scales: p * scale of
-      // each PV group as a bf16 pair hi + lo, planes [g0 | g1] and [g2 | g3],
-      // each group's row part [hi 0..7 | hi 8..15 | lo 0..7 | lo 8..15]).
+      // a6 operand: P^T into buffer b % kPBufs.
       const int pbi = b % kPBufs;
       if (b >= kPBufs) W.wait(bar(kBarPEmpty + pbi), ((b / kPBufs) - 1) & 1);  // PV read it
-      if (kGroup) {
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const float scg = scp[g];
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float v0 = pe[2 * k] * scg, v1 = pe[2 * k + 1] * scg;
-            hi[k] = pack_bf16(v0, v1);
-            lo[k] = pack_bf16(v0 - __uint_as_float(hi[k] << 16),
-                              v1 - __uint_as_float(hi[k] & 0xFFFF0000u));
-          }
-          uint8_t* prow = sm + kOffP + (g >> 1) * kPPlaneBytes + p_row;
-          const uint32_t c_hi = 4u * (uint32_t)(g & 1) + (uint32_t)hf;
-          *reinterpret_cast<uint4*>(prow + ((c_hi ^ p_sw) << 4)) =
-              make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(prow + (((c_hi + 2u) ^ p_sw) << 4)) =
-              make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
-      } else {
+      {
         uint8_t* prow = sm + kOffP + pbi * kPPlaneBytes + p_row;
         *reinterpret_cast<uint4*>(prow + (((uint32_t)hf ^ p_sw) << 4)) =
             make_uint4(pack_bf16(pe[0], pe[1]), pack_bf16(pe[2], pe[3]),
@@ -695,8 +506,8 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
           __syncwarp();
           tc_fence_after();
 #pragma unroll
-          for (int c = 0; c < (kGroup ? 8 : 4); ++c) {   // 16-column pieces (hi, lo)
-            const uint32_t col = kColO + (kGroup ? 16u * (uint32_t)c : 32u * (uint32_t)c);
+          for (int c = 0; c < 4; ++c) {                  // the 16 head columns of block c
+            const uint32_t col = kColO + 32u * (uint32_t)c;
             uint32_t w[16];
             tmem_ld16(tmem + lane_base + col, w);
             tmem_wait_ld();
@@ -737,12 +548,11 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
       W.wait(bar(kBarOFinal), 0);
       tc_fence_after();
     }
-    const float oscale = kFmt == kE4m3 ? kscale : 1.f;
     float inv[kN];
 #pragma unroll
     for (int hd = 0; hd < kN; ++hd) {
       const float l = hsh[kN + hd];
-      inv[hd] = (!(l > 0.f) || nb == 0) ? 0.f : oscale / l;
+      inv[hd] = (l == 0.f || nb == 0) ? 0.f : __fdividef(1.f, l);
     }
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -752,14 +562,6 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
       __syncwarp();
       if (nb > 0) {
         tmem_ld16(tmem + lane_base + kColO + 32u * (uint32_t)c, w);
-        if (kGroup) {                                   // O = hi part + lo part
-          uint32_t w2[16];
-          tmem_ld16(tmem + lane_base + kColO + 32u * (uint32_t)c + 16u, w2);
-          tmem_wait_ld();
-#pragma unroll
-          for (int hd = 0; hd < kN; ++hd)
-            w[hd] = __float_as_uint(__uint_as_float(w[hd]) + __uint_as_float(w2[hd]));
-        }
         tmem_wait_ld();
       }
       const int ch = 128 * c + row;                   // output channel of lane `row`
@@ -778,7 +580,7 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
     // Thread `row` < h writes head row's LSE.
     if (row < p.h) {
       const float mi = hsh[2 * kN + row], li = hsh[kN + row];
-      const bool empty = !(li > 0.f) || nb == 0;
+      const bool empty = li == 0.f || nb == 0;   // (a NaN row sum is not empty)
       const float lse_v = empty ? -INFINITY : (mi + log2f(li)) * 0.69314718055994530942f;
       const int64_t orow = (int64_t)t * p.h + row;
       if (p.fp32_out)
@@ -798,10 +600,9 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
   }
 }
 
-template <int kFmt>
 cudaError_t launch_keys(const KeysArgs& a, unsigned blocks, cudaStream_t stream) {
   const bool lpt = a.p.lpt && blocks <= (unsigned)kLptMaxUnits;
-  auto kernel = lpt ? smla_tc_keys_kernel<kFmt, true> : smla_tc_keys_kernel<kFmt, false>;
+  auto kernel = lpt ? smla_tc_keys_kernel<true> : smla_tc_keys_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -814,30 +615,20 @@ cudaError_t launch_keys(const KeysArgs& a, unsigned blocks, cudaStream_t stream)
 int tc_keys_max_range() { return kMaxBlocks * kBK; }
 
 bool tc_keys_supported(int h, int d_qk, int kv_format) {
-  if (h < 1 || h > kN || (d_qk != 576 && d_qk != 512)) return false;
-  if (kv_format == kDsMla || kv_format == kE4m3Group4Kpe) return d_qk == 576;
-  return kv_format == kBf16 || kv_format == kE4m3 || kv_format == kE4m3Group;
+  return h >= 1 && h <= kN && (d_qk == 576 || d_qk == 512) && kv_format == kBf16;
 }
 
 cudaError_t launch_tc_keys(const FwdParams& p, cudaStream_t stream) {
   KeysArgs a{};
   a.p = p;
-  if (p.kv_format == kBf16) {
-    const cudaError_t e = encode_bf16_rows_map(&a.kv_map, p.kv, p.d_qk, p.num_slots);
-    if (e != cudaSuccess) return e;
-  }
+  if (p.kv_format != kBf16) return cudaErrorInvalidValue;   // (the plan sends only bf16)
+  const cudaError_t e = encode_bf16_rows_map(&a.kv_map, p.kv, p.d_qk, p.num_slots);
+  if (e != cudaSuccess) return e;
   a.ksteps = p.d_qk == 576 ? 18 : 16;
-  a.G = (p.d_qk + 127) / 128;
   a.scale_log2 = p.sm_scale * 1.4426950408889634f;
   const int64_t blocks = (int64_t)p.T * p.splits;    // one CTA per unit
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  switch (p.kv_format) {
-    case kBf16: return launch_keys<kBf16>(a, (unsigned)blocks, stream);
-    case kE4m3: return launch_keys<kE4m3>(a, (unsigned)blocks, stream);
-    case kE4m3Group: return launch_keys<kE4m3Group>(a, (unsigned)blocks, stream);
-    case kDsMla: return launch_keys<kDsMla>(a, (unsigned)blocks, stream);
-    default:    return launch_keys<kE4m3Group4Kpe>(a, (unsigned)blocks, stream);
-  }
+  return launch_keys(a, (unsigned)blocks, stream);
 }
 
 }  // namespace smla
