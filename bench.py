@@ -62,6 +62,8 @@ def flops_of(w) -> float:
 
 
 def row_bytes(w) -> int:
+    if w.kv_dtype == W.KV_FP8_DS_MLA:
+        return 656                      # 512 E4M3 + 4 fp32 scales + 64 bf16
     return 2 * w.d_qk if w.kv_dtype == W.KV_BF16 else w.d_qk
 
 
@@ -69,7 +71,8 @@ def bytes_model(w):
     """Algorithmic bytes: per-token terms (q, O, LSE, indices, valid) plus the
     selected rows once per token (G) or once overall (U)."""
     G = (w.d_qk + 127) // 128
-    scale_b = 4 * G if w.kv_dtype == W.KV_FP8_E4M3_GROUP128 else 0
+    scale_b = 4 * G if w.kv_dtype == W.KV_FP8_E4M3_GROUP128 else \
+        16 if w.kv_dtype == W.KV_FP8_E4M3_GROUP4_KPE else 0
     per_tok = w.T * (2 * w.h * w.d_qk + 2 * w.h * w.d_v + 4 * w.h
                      + 4 * w.topk + 4)
     v = w.valid_len.clamp(0, w.topk)
@@ -352,7 +355,7 @@ def run_ours(args, rank, world, local_rank):
     # ---- secondary: bf16 decode ----------------------------------------------
     secondary = {}
     if not args.no_secondary:
-        for name in ["bf16_decode", "fp8_nope_decode", "mixed_fp8_group"]:
+        for name in ["bf16_decode", "fp8_nope_decode", "mixed_fp8_group", "ds_mla_decode"]:
             w2, ws2, out2, lse2, n2 = setup(name, rank)
             f2 = step_fn(w2, ws2, out2, lse2)
             with torch.cuda.stream(stream):

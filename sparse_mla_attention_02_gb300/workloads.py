@@ -254,12 +254,39 @@ def mixed_fp8_group(device="cpu", seed=1004, n_req=32, tok_per_req=512,
                     torch.from_numpy(valid).to(device), h)
 
 
+def ds_mla_decode(device="cpu", seed=1005, T=128, h=128, per_req=16384,
+                  scale_range=(0.01, 0.1)) -> Workload:
+    """Decode on the 656-byte fp8_ds_mla cache: one token per request, 128
+    heads, 2048 distinct slots from its own request's 16384; the shape of the
+    pages' FP8 FlashMLA decode (heads padded to 128, fp8_ds_mla rows), with
+    the rows drawn like the other FP8 caches (E4M3 of N(0,1)/scale, scales
+    ~U[0.01, 0.1] per 128-channel group, bf16 N(0,1) rope)."""
+    d_qk, d_v, topk = 576, 512, 2048
+    S = T * per_req
+    g = _gen(device, seed)
+    rng = np.random.default_rng(seed)
+    q = bf16_normal((T, h, d_qk), device, g)
+    lo, hi = scale_range
+    scales = (torch.rand((S, 4), generator=g, device=device) * (hi - lo) + lo).float()
+    codes = fp8_cache_group(S, 512, scales, device, g)
+    kv = ds_mla_rows(codes, scales, bf16_normal((S, 64), device, g))
+    del codes
+    valid = np.full(T, topk, dtype=np.int32)
+    idx = index_rows(rng, T, topk, valid, lambda t, v: t * per_req +
+                     rng.choice(per_req, v, replace=False))
+    return Workload("ds_mla_decode", T, h, d_qk, d_v, topk, S, KV_FP8_DS_MLA,
+                    1.0 / math.sqrt(576), q, kv, None,
+                    torch.from_numpy(idx).to(device),
+                    torch.from_numpy(valid).to(device), h)
+
+
 CONFIGS = {
     "tiny": tiny,
     "bf16_decode": bf16_decode,
     "fp8_nope_decode": fp8_nope_decode,
     "bf16_prefill": bf16_prefill,
     "mixed_fp8_group": mixed_fp8_group,
+    "ds_mla_decode": ds_mla_decode,      # secondary: not one of the five configs
 }
 
 
