@@ -51,7 +51,7 @@ def test_stalled_wait_reports_timeout_and_the_next_launch_is_clean(cuda_lib, nam
     w = W.custom(name=name, **kw)
     wd = w.to("cuda")
     Or, Lr = oracle_fwd(w)
-    assert smla.smla_get_device_status(clear=True) in (0, SMLA_ERR_TIMEOUT)
+    smla.smla_get_device_status(clear=True)       # earlier tests may leave bits set
     smla.smla_test_set_stall(True, 2000)          # 2 ms per wait
     try:
         _run(smla, wd)                            # returns; outputs undefined
