@@ -21,7 +21,6 @@ from __future__ import annotations
 
 import argparse
 import hashlib
-import glob
 import json
 import os
 import statistics
@@ -82,24 +81,33 @@ def bytes_model(w):
     return per_tok + uniq * (row_bytes(w) + scale_b), per_tok + gathered
 
 
-def csrc_digest() -> str:
+# The sources each kernel is built from: a traffic figure measured on a
+# kernel stays valid while these files are unchanged.
+KERNEL_SOURCES = {
+    "tc_heads": ("smla_tc.cu", "tc_common.cuh", "tc_ptx.cuh", "smla_internal.h"),
+    "tc_keys": ("smla_tc_keys.cu", "tc_common.cuh", "tc_ptx.cuh", "smla_internal.h"),
+    "tc_keys_fp8": ("smla_tc_fp8.cu", "tc_common.cuh", "tc_ptx.cuh", "smla_internal.h"),
+    "cache_write": ("smla_cache.cu", "smla_internal.h"),
+}
+
+
+def sources_digest(kernel: str) -> str:
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "sparse_mla_attention_02_gb300",
-                                           "csrc", "*"))):
-        with open(p, "rb") as f:
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "sparse_mla_attention_02_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel_key: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
+def ncu_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu summary
+    (profiles/traffic.json), if it was taken on the current sources of that
+    kernel (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            d = json.load(f)
-        e = d[kernel_key]
-        if e.get("csrc_sha") == csrc_digest():
+            e = json.load(f)[workload]
+        if e.get("kernel") == kernel and e.get("sources_sha") == sources_digest(kernel):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -250,6 +258,49 @@ def run_ours(args, rank, world, local_rank):
     def ranks_max(x):
         return max_over_ranks(x, world, dev)
 
+    def cache_write_bench():
+        """The group-quantizing E4M3 cache write: 131072 token rows
+        [kv_c | k_pe] (bf16, 151 MB) to random slots of a 262144-slot cache;
+        per row 1152 B read + 576 B codes + 20 B scales written + 4 B slot
+        id (1752 B), more than L2 per launch."""
+        Ncw, Scw = 131072, 262144
+        gcw = torch.Generator(device=dev).manual_seed(4242 + 7919 * rank)
+        kv_c = torch.randn((Ncw, 512), generator=gcw, device=dev).to(torch.bfloat16)
+        k_pe = torch.randn((Ncw, 64), generator=gcw, device=dev).to(torch.bfloat16)
+        slots = torch.randperm(Scw, generator=gcw, device=dev)[:Ncw].int().contiguous()
+        cache = torch.empty((Scw, 576), dtype=torch.uint8, device=dev)
+        scales = torch.empty((Scw, 5), dtype=torch.float32, device=dev)
+
+        def f4():
+            smla.smla_cache_write_e4m3_group(kv_c, k_pe, slots, cache, scales, stream=stream)
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                f4()
+        stream.synchronize()
+        barrier()
+        k4 = max(args.steps, 20)
+        t4 = ranks_max(time_steps(f4, k4, stream)) / k4
+        b4 = Ncw * (2 * 576 + 576 + 4 * 5 + 4)
+        res = {
+            "rows_per_s": round(world * Ncw / t4, 1),
+            "ms_per_step": round(1e3 * t4, 4),
+            "hbm_gbs": round(b4 / t4 / 1e9, 1),
+            "frac_hbm": round(b4 / t4 / 1e9 / pk["hbm_gbs"], 4),
+            "bytes_per_row": 1752,
+            "bytes_per_launch": b4,
+            "traffic": ncu_traffic("fp8_group_cache_write", "cache_write"),
+            "kernel": "smla_cache_write_kernel",
+        }
+        del kv_c, k_pe, slots, cache, scales
+        torch.cuda.empty_cache()
+        return res
+
+    if args.cache_write_only:
+        res = cache_write_bench()
+        if rank == 0:
+            print(json.dumps({"config": "fp8_group_cache_write", **res}))
+        return
+
     # ---- headline: bf16 prefill --------------------------------------------
     w, ws, out, lse, ws_n = setup(args.config, rank, args.tokens)
     fl = flops_of(w)
@@ -283,7 +334,8 @@ def run_ours(args, rank, world, local_rank):
         "peak": pk["bf16_tflops"] if bound_tensor else pk["hbm_gbs"],
         "unit": "TFLOP/s" if bound_tensor else "GB/s",
         "peak_source": f"{pk_src} ({'bf16 burst' if bound_tensor else 'copy'})",
-        "traffic": ncu_traffic(args.config),
+        "traffic": ncu_traffic(args.config, smla.smla_plan_info(
+            w.T, w.h, w.d_qk, w.topk, w.kv_dtype)["kernel"]),
         "algorithmic_flops_per_launch": fl,
         "algorithmic_bytes_per_launch": {"U": U, "G": G},
     }
@@ -384,7 +436,8 @@ def run_ours(args, rank, world, local_rank):
                 "frac_hbm_G": round(G2 / t2 / 1e9 / pk["hbm_gbs"], 4),
                 "frac_hbm_G_cold_l2": round(G2 / tc2 / 1e9 / pk["hbm_gbs"], 4),
                 "bytes_per_launch": {"U": U2, "G": G2},
-                "traffic": ncu_traffic(name),
+                "traffic": ncu_traffic(name, smla.smla_plan_info(
+                    w2.T, w2.h, w2.d_qk, w2.topk, w2.kv_dtype)["kernel"]),
                 "splits_workspace_bytes": n2,
                 "kernel": smla.smla_plan_info(w2.T, w2.h, w2.d_qk, w2.topk,
                                               w2.kv_dtype)["kernel"],
@@ -428,38 +481,7 @@ def run_ours(args, rank, world, local_rank):
             del w2, ws2, out2, lse2
             torch.cuda.empty_cache()
 
-        # ---- secondary: group-quantizing E4M3 cache write --------------------
-        # 131072 token rows [kv_c | k_pe] (bf16, 151 MB) written to random
-        # slots of a 262144-slot cache; per row 1152 B read + 576 B codes +
-        # 20 B scales written + 4 B slot id (1752 B), more than L2 per launch.
-        Ncw, Scw = 131072, 262144
-        gcw = torch.Generator(device=dev).manual_seed(4242 + 7919 * rank)
-        kv_c = torch.randn((Ncw, 512), generator=gcw, device=dev).to(torch.bfloat16)
-        k_pe = torch.randn((Ncw, 64), generator=gcw, device=dev).to(torch.bfloat16)
-        slots = torch.randperm(Scw, generator=gcw, device=dev)[:Ncw].int().contiguous()
-        cache = torch.empty((Scw, 576), dtype=torch.uint8, device=dev)
-        scales = torch.empty((Scw, 5), dtype=torch.float32, device=dev)
-
-        def f4():
-            smla.smla_cache_write_e4m3_group(kv_c, k_pe, slots, cache, scales, stream=stream)
-        with torch.cuda.stream(stream):
-            for _ in range(args.warmup):
-                f4()
-        stream.synchronize()
-        barrier()
-        k4 = max(args.steps, 20)
-        t4 = ranks_max(time_steps(f4, k4, stream)) / k4
-        b4 = Ncw * (2 * 576 + 576 + 4 * 5 + 4)
-        secondary["fp8_group_cache_write"] = {
-            "rows_per_s": round(world * Ncw / t4, 1),
-            "ms_per_step": round(1e3 * t4, 4),
-            "hbm_gbs": round(b4 / t4 / 1e9, 1),
-            "frac_hbm": round(b4 / t4 / 1e9 / pk["hbm_gbs"], 4),
-            "bytes_per_row": 1752,
-            "kernel": "smla_cache_write_kernel",
-        }
-        del kv_c, k_pe, slots, cache, scales
-        torch.cuda.empty_cache()
+        secondary["fp8_group_cache_write"] = cache_write_bench()
     del flush
 
     if rank == 0:
@@ -615,6 +637,8 @@ def main():
                     help="use only the last N tokens of the config (profiling)")
     ap.add_argument("--main-only", action="store_true",
                     help="time only the main step loop (profiling)")
+    ap.add_argument("--cache-write-only", action="store_true",
+                    help="time only the E4M3 group cache write (profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
