@@ -794,7 +794,8 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
                                      fmaxf(red_sc[8 + gg], red_sc[12 + gg]));
               if (ms > 0.f && (R[gg] == 0.f || ms * R[gg] > 1.f)) {
                 const float rn = pow2_at_most_inv(ms);
-                if (R[gg] != 0.f) ratio[gg] = rn * __frcp_rn(R[gg]);   // powers of two: exact
+                if (R[gg] != 0.f)                   // powers of two: exact
+                  ratio[gg] = rn * __uint_as_float(0x7F000000u - (__float_as_uint(R[gg]) & 0x7F800000u));
                 R[gg] = rn;
               }
             }
@@ -900,22 +901,44 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
         tmem_ld8(col + 16, wl8);
         tmem_wait_ld();
         const float rc = kGroup ? R[c] : 1.f;
-        const float rinv = rc > 0.f ? __frcp_rn(rc) : 0.f;   // (a power of two: exact)
+        // 1 / R_c: R_c is a power of two (or 0: no key of the unit has a
+        // nonzero scale in this group), so the reciprocal is exact from the
+        // exponent field
+        const float rinv =
+            rc > 0.f ? __uint_as_float(0x7F000000u - (__float_as_uint(rc) & 0x7F800000u)) : 0.f;
         const int ch = 128 * c + key;                   // output channel of lane `key`
+        float ov[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           // (no valid key for the head, or none with a nonzero scale in this
           // group: 0 exactly)
-          const float o = (l_tot[i] != 0.f && rinv > 0.f)
-                              ? fmaf(__uint_as_float(wl8[i]), 0.0625f, __uint_as_float(wh[i])) *
-                                    (inv[i] * rinv)
-                              : 0.f;
-          if (!p.fp32_out) {
-            ost[(8 * wg + i) * 512 + ch] = __float2bfloat16_rn(o);
-          } else if (head_ok[i]) {
-            const int64_t orow = (int64_t)ui.t * p.h + ui.h0 + 8 * wg + i;
-            p.o_part[((int64_t)ui.split * p.T * p.h + orow) * p.d_v + ch] = o;
+          ov[i] = (l_tot[i] != 0.f && rinv > 0.f)
+                      ? fmaf(__uint_as_float(wl8[i]), 0.0625f, __uint_as_float(wh[i])) *
+                            (inv[i] * rinv)
+                      : 0.f;
+        }
+        if (!p.fp32_out) {
+          // lanes 2m and 2m + 1 hold channels ch, ch + 1: the even lane stores
+          // heads 0..3 of both, the odd lane heads 4..7, as bf16 pairs
+          const bool odd = (lane & 1) != 0;
+          const int ch0 = ch & ~1;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float send = odd ? ov[i] : ov[i + 4];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+            const int hd = odd ? i + 4 : i;
+            const float lo = odd ? recv : ov[i];          // channel ch0
+            const float hi = odd ? ov[i + 4] : recv;      // channel ch0 + 1
+            *reinterpret_cast<__nv_bfloat162*>(ost + (8 * wg + hd) * 512 + ch0) =
+                __floats2bfloat162_rn(lo, hi);
           }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (head_ok[i]) {
+              const int64_t orow = (int64_t)ui.t * p.h + ui.h0 + 8 * wg + i;
+              p.o_part[((int64_t)ui.split * p.T * p.h + orow) * p.d_v + ch] = ov[i];
+            }
         }
       }
       // (the TMEM loads of O are complete: the next unit's first PV, which
