@@ -240,18 +240,9 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
                     t * 128, bar(kBarQLoaded));
     }
   }
-  __syncwarp();
-  if (warp == 0) {
-    tmem_alloc(sb + kOffTmemSlot, kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  cluster_arrive();
-  cluster_wait();
-  tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + kOffTmemSlot);
-
-  // a1/a2 setup: the producers read the whole index range of the unit once
+  // a1/a2 setup (before the TMEM allocation and the cluster barrier, which
+  // it does not need, so that the loads overlap them): the producers read
+  // the whole index range of the unit once
   // (coalesced, all loads in flight together) into shared memory, masking
   // positions past k1, ids < 0 and ids >= num_slots; then one valid-mask per
   // block.  Every role reads both from shared memory afterwards.
@@ -263,15 +254,42 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
     if (load_unit_slots(p, t, k0, k1, n, slots, pt, kProducers))
       atomicCAS(p.status, 0, kStatusBadIndex);
     named_bar_sync(1, kProducers);
-    if (warp < 3) {                        // warp 1: rows 0..31, warp 2: rows 32..47
-      const int row = (warp - 1) * 32 + lane;
-      for (int b = 0; b < nb; ++b) {
-        const bool ok = row < kBN && slots[b * kBN + row] >= 0;
-        const uint32_t m = __ballot_sync(0xffffffffu, ok);
-        if (lane == 0) masks[b * 2 + (warp - 1)] = m;
+    // One valid-mask pair per block (rows 0..31, rows 32..47): the three
+    // warps take every third block, four blocks per step (their slot-id
+    // reads in flight together).
+    {
+      const int w = warp - 1;
+      for (int b0 = 4 * w; b0 < nb; b0 += 12) {
+        int id0[4], id1[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int b = min(b0 + k, nb - 1);
+          id0[k] = slots[b * kBN + lane];
+          id1[k] = lane < kBN - 32 ? slots[b * kBN + 32 + lane] : -1;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t m0 = __ballot_sync(0xffffffffu, id0[k] >= 0);
+          const uint32_t m1 = __ballot_sync(0xffffffffu, id1[k] >= 0);
+          if (lane == 0 && b0 + k < nb) {
+            masks[(b0 + k) * 2] = m0;
+            masks[(b0 + k) * 2 + 1] = m1;
+          }
+        }
       }
     }
   }
+  __syncwarp();
+  if (warp == 0) {
+    tmem_alloc(sb + kOffTmemSlot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  cluster_arrive();
+  cluster_wait();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + kOffTmemSlot);
+
   __syncthreads();
 
   if (warp == 0) {
