@@ -708,26 +708,32 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
       // 16-byte stores would each touch half a sector of a different row).
       uint8_t* box0 = sm + kOffTile + (uint32_t)(2 * wg) * 16384u + (uint32_t)head * 128u;
       const uint32_t hsw = (uint32_t)head & 7u;
+      // (32 channels per TMEM wait)
 #pragma unroll 1
-      for (int c = 0; c < 128; c += 16) {
-        uint32_t w[16];
+      for (int c2 = 0; c2 < 128; c2 += 32) {
+        uint32_t w[2][16];
         __syncwarp();
         if (nb > 0) {
-          tmem_ld16(tmem + lane_base + kColO + 128 * wg + c, w);
+          tmem_ld16(tmem + lane_base + kColO + 128 * wg + c2, w[0]);
+          tmem_ld16(tmem + lane_base + kColO + 128 * wg + c2 + 16, w[1]);
           tmem_wait_ld();
         }
-        uint32_t o[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          o[k] = empty ? 0u
-                       : pack_bf16(__uint_as_float(w[2 * k]) * inv,
-                                   __uint_as_float(w[2 * k + 1]) * inv);
-        const uint32_t ck = (uint32_t)(c >> 3);             // 16-byte chunk of the 128 channels
-        uint8_t* brow = box0 + (ck >> 3) * 16384u;
-        *reinterpret_cast<uint4*>(brow + ((((ck & 7u) + 0u) ^ hsw) << 4)) =
-            make_uint4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<uint4*>(brow + ((((ck & 7u) + 1u) ^ hsw) << 4)) =
-            make_uint4(o[4], o[5], o[6], o[7]);
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int c = c2 + 16 * h2;
+          uint32_t o[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            o[k] = empty ? 0u
+                         : pack_bf16(__uint_as_float(w[h2][2 * k]) * inv,
+                                     __uint_as_float(w[h2][2 * k + 1]) * inv);
+          const uint32_t ck = (uint32_t)(c >> 3);           // 16-byte chunk of the 128 channels
+          uint8_t* brow = box0 + (ck >> 3) * 16384u;
+          *reinterpret_cast<uint4*>(brow + ((((ck & 7u) + 0u) ^ hsw) << 4)) =
+              make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(brow + ((((ck & 7u) + 1u) ^ hsw) << 4)) =
+              make_uint4(o[4], o[5], o[6], o[7]);
+        }
       }
       fence_proxy_async_smem();
       named_bar_sync(nbar, 128);
@@ -788,8 +794,11 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
   // barriers first.
   // (also after an abort: the peer's shared memory stays until the cluster
   // barrier below, which this CTA passes only after its copies are complete)
-  // (and the O boxes' TMA stores have read the staging)
-  if (tid == 128 || tid == 256) bulk_wait_all();
+  // (and the O boxes' TMA stores have read the staging: only the reads of
+  // this CTA's shared memory need to be complete before it leaves; the sends
+  // have landed in the peer, which consumed them before its last X-free
+  // arrival waited on below)
+  if (tid == 128 || tid == 256) bulk_wait_read_all();
   if (tid == 0 && a.q_tma) W.drain(bar(kBarQLoaded), 0);
   if (tid == 128 && nb > 0) {
     if (nb >= 2) W.wait(bar(kBarXFree + ((nb - 2) & 1)), ((nb - 2) >> 1) & 1);
