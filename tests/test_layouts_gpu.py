@@ -2,9 +2,10 @@
 
 * The 656-byte fp8_ds_mla row (512 E4M3 ckv bytes, four fp32 group scales,
   64 bf16 rope values in one row) and E4M3 with four ckv group scales plus a
-  separate kpe scale, on every kernel that serves them: the keys-major
-  tensor-core kernel (h <= 16, also with a split top-k range) and the
-  CUDA-core kernel (h > 16).  Bar: max|dO| <= 2e-2, max|dLSE| <= 1e-3.
+  separate kpe scale, on the kernel that serves them (the E4M3-operand
+  keys-major kernel, in groups of 16 heads: one group, several groups with
+  a partial last one, and a split top-k range).  Bar: max|dO| <= 2e-2,
+  max|dLSE| <= 1e-3.
 * The split query (q_nope, q_pe): smla_fwd_split_q must give exactly what
   smla_fwd gives on the concatenated q, on every kernel family, because the
   kernels read the same values from two places.
@@ -22,13 +23,15 @@ from tests.test_parity_gpu import compare
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    # keys-major kernel: several 128-key blocks, a partial block, empty rows
+    # one group of 16 heads: several 128-key blocks, a partial block, empty rows
     dict(T=6, h=16, topk=400, num_slots=2000, valid=[400, 257, 128, 1, 0, 129]),
     dict(T=3, h=5, topk=128, num_slots=300, valid=[128, 60, 2]),
-    # keys-major kernel with a split top-k range (few tokens, long rows)
+    # a split top-k range (few tokens, long rows)
     dict(T=2, h=16, topk=2048, num_slots=6000, valid=[2048, 1500]),
-    # CUDA-core kernel (h > 16)
+    # several groups of 16 heads, the last one partial (h = 17, 32, 64, 128)
+    dict(T=3, h=17, topk=160, num_slots=600, valid=[160, 129, 0]),
     dict(T=4, h=32, topk=96, num_slots=500, valid=[96, 40, 1, 0]),
+    dict(T=3, h=64, topk=256, num_slots=900, valid=[256, 100, 3]),
     dict(T=2, h=128, topk=64, num_slots=300, valid=[64, 33]),
 ]
 

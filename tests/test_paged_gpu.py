@@ -3,8 +3,9 @@ slots inside the kernels' index loads) with the fp64 oracle on the converted
 ids, and with smla_fwd on the same slots: the two calls must agree bit for
 bit, because the same kernels read the same rows.
 
-Covers every kernel family (heads-major bf16 and E4M3, keys-major with group
-scales, the CUDA-core path), a split top-k range, a block stride larger than
+Covers every kernel family (heads-major bf16 and E4M3, the E4M3-operand
+keys-major kernel with group scales for one and for several groups of 16
+heads), a split top-k range, a block stride larger than
 the block size, and the entries the translation masks (pages past the
 table, unallocated blocks, a request id outside the table).
 """
@@ -71,11 +72,14 @@ def check_oracle(w, O, L, glob):
 CASES = [
     # heads-major tensor-core kernel, bf16, several blocks, empty rows
     dict(T=12, h=128, topk=256, num_slots=3000, valid=[256, 0, 5, 200, 48, 49, 1, 96, 97, 150, 256, 7]),
-    # heads-major, per-tensor E4M3, NoPE rows, h padded
+    # per-tensor E4M3, NoPE rows, h = 64 (the E4M3-operand kernel, four
+    # groups of 16 heads)
     dict(T=6, h=64, d_qk=512, topk=300, num_slots=900, kv_dtype=1, valid=[300, 257, 33, 2, 1, 0]),
-    # keys-major tensor-core kernel, E4M3 with group scales
+    # per-tensor E4M3 with h = 80 (the heads-major kernel, converting loaders)
+    dict(T=3, h=80, topk=200, num_slots=700, kv_dtype=1, valid=[200, 64, 1]),
+    # E4M3 with group scales, one group of 16 heads
     dict(T=5, h=16, topk=400, num_slots=2000, kv_dtype=2, valid=[400, 130, 1, 0, 255]),
-    # CUDA-core path (group scales with h > 16)
+    # E4M3 with group scales, two groups of 16 heads
     dict(T=4, h=32, topk=128, num_slots=700, kv_dtype=2, valid=[128, 64, 3, 0]),
     # split top-k ranges (few tokens, long rows): partials + combine
     dict(T=2, h=128, topk=2048, num_slots=8192, valid=[2048, 1300]),

@@ -79,8 +79,12 @@ def test_tiny_config(cuda_lib):
     assert dO <= TOL_O and dL <= TOL_LSE
 
 
+# (h = 17 and 65 sit on the plan's boundaries: bf16 moves from the
+# keys-major to the heads-major kernel above 16 heads, E4M3 group formats
+# take a second group of 16 heads, and a per-tensor E4M3 cache moves from the
+# E4M3-operand kernel to the heads-major one above 64 heads)
 @pytest.mark.parametrize("kv_dtype", [0, 1, 2])
-@pytest.mark.parametrize("h", [1, 16, 48, 64, 128])
+@pytest.mark.parametrize("h", [1, 16, 17, 48, 64, 65, 128])
 def test_heads_and_formats(cuda_lib, kv_dtype, h):
     w = W.custom(T=5, h=h, topk=200, num_slots=700, kv_dtype=kv_dtype,
                  valid=[200, 131, 64, 1, 0], seed=100 + h + kv_dtype,
