@@ -17,11 +17,21 @@
 //     2^-a (S_hi + S_lo / 16), summed in fp32.
 //   * P (fp32, in [0, 2^4] by the lazy running max below): with group
 //     scales, each V group g gets x = p * scale_g * R_g * 2^4, R_g a power
-//     of two that keeps scale_g * R_g <= 1, split the same way into hi and
-//     lo * 16 columns of the PV operand; O = (O_hi + O_lo / 16) / (16 R_g l).
+//     of two that keeps scale_g * R_g <= 1, split into three E4M3 terms,
+//     x = hi + mid / 16 + lo / 256 (mid = E4M3(16 (x - hi)), lo the same
+//     of the next residual), up to 2^-11 of |x| (the f16 step of the split)
+//     plus 2^-13.  Every key's weight carries its scale, so every key has
+//     this error, the heaviest one too; with two terms (2^-9) a row that
+//     one key carries with |v| near 4 came out 0.0208 from the oracle
+//     (the output's own bf16 rounding takes up to 0.0156 of the 2e-2 bound
+//     there).  The three are the 48 columns [hi | mid | lo] of the PV
+//     operand; O = (O_hi + O_mid / 16 + O_lo / 256) / (16 R_g l).  With one
+//     scale per tensor x = 16 p: the heaviest key's weight is exact (p = 1
+//     at the running max), as with a bf16 P, and two terms [hi | lo] (32
+//     columns) carry the others.
 // Keys are the MMA's M dimension (keys-major), heads its N:
 //   S^T[keys, 32] = K[keys, d] . Q'^T[d, 32]      A = gathered tile, K-major
-//   O^T[ch, 32]  += V^T[ch, keys] . P'^T[keys, 32] A = the same tile, MN-major
+//   O^T[ch, 48]  += V^T[ch, keys] . P'^T[keys, 48] A = the same tile, MN-major
 // A block is 128 keys (M = 128), full 576-byte rows in five 128-byte chunks
 // (four ckv chunks and the rope chunk; for the 656-byte row the rope chunk
 // holds its 64 bf16 values and its QK runs as a bf16 MMA).  With group
@@ -42,10 +52,11 @@
 //   a4 QK^T, a5 masked online softmax, a6 PV, a7 O / l and LSE = m + ln l
 //
 // Warp roles (448 threads): warp 0 issues the QK MMAs and owns TMEM; warp 13
-// issues the PV MMAs; warps 1..4 load the unit's slot ids, then issue the
-// gathers (each 32 tile rows); warps 5..12 are two softmax warpgroups
-// (thread <-> key <-> TMEM lane; warpgroup w owns heads [8w, 8w + 8)), which
-// also build Q' and write O and LSE.
+// issues the PV MMAs; warps 1..4 load the unit's slot ids, issue the
+// gathers (each 32 tile rows) and build Q' of every unit after the first;
+// warps 5..12 are two softmax warpgroups (thread <-> key <-> TMEM lane;
+// warpgroup w owns heads [8w, 8w + 8)), which build the first unit's Q' and
+// write O and LSE.
 // Every wait is bounded; a wait that runs out records a timeout status, sets
 // an abort flag that skips later waits, and the block drains its copies and
 // MMAs and finishes normally.
@@ -75,7 +86,8 @@ constexpr int kStageBytes = kMaxChunks * kChunkBytes;
 constexpr int kHeads = 16;                 // heads per CTA
 constexpr int kNq = 32;                    // QK N: 16 heads hi | 16 heads lo
 constexpr int kQChunkBytes = kNq * 128;
-constexpr int kPBytes = kBK * 128;         // P': one 128-byte row per key
+constexpr int kPBytes = kBK * 128;         // one P' region: a 128-byte row per key
+constexpr int kNoMax = 48;                 // PV N: 16 heads hi | mid | lo (group scales)
 constexpr int kThreads = 448;
 constexpr int kProducers = 128;            // warps 1..4
 constexpr int kSoftmax = 256;              // warps 5..12
@@ -84,11 +96,12 @@ constexpr float kT = 4.f;                  // lazy max threshold (log2 units)
 constexpr float kPShift = 16.f;            // 2^(8 - kT): P' <= 2^8
 
 // TMEM columns.
-constexpr uint32_t kColO = 0;              // O^T: 4 blocks of 128 channels x 32
-constexpr uint32_t kColS = 128;            // S: 2 buffers x 5 accumulators x 32
+// O^T: 4 blocks of 128 channels x (48 or 32) from column 0, then S: 2
+// buffers x 5 accumulators x 32.
+constexpr uint32_t kColO = 0;
 constexpr uint32_t kSBuf = 5 * kNq;
 constexpr uint32_t kTmemCols = 512;
-static_assert(kColS + 2 * kSBuf <= kTmemCols, "TMEM budget");
+static_assert(4 * kNoMax + 2 * kSBuf <= kTmemCols, "TMEM budget");
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).  The tile
 // stages carry, beside the rows, each block's valid-bit words and (group
@@ -96,15 +109,20 @@ static_assert(kColS + 2 * kSBuf <= kTmemCols, "TMEM budget");
 constexpr int kScaleRow = 5;                                       // floats per key
 constexpr uint32_t kOffTile = 0;
 constexpr uint32_t kOffQ = kOffTile + kStages * kStageBytes;       // Q' chunks
-constexpr uint32_t kOffP = kOffQ + kMaxChunks * kQChunkBytes;      // P' (one buffer)
-constexpr uint32_t kOffSlot = kOffP + kPBytes;                     // [blocks*128] i32
+// P' (one buffer, two regions: groups 0, 1 and groups 2, 3; one scale per
+// tensor uses region 0 only); the bf16 O staging rows [16 heads][512] share
+// region 1 (written once the unit's last PV has read P', and read by a bulk
+// copy that completes before the next unit's first P' is written).
+constexpr uint32_t kOffP = kOffQ + kMaxChunks * kQChunkBytes;
+constexpr uint32_t kOffOst = kOffP + kPBytes;
+constexpr uint32_t kOffSlot = kOffP + 2 * kPBytes;                 // [blocks*128] i32
 constexpr uint32_t kOffSc = kOffSlot + kMaxBlocks * kBK * 4;       // [2][128][5] f32
 constexpr uint32_t kOffMask = kOffSc + kStages * kBK * kScaleRow * 4;  // [2][4] u32
 constexpr uint32_t kOffRed = kOffMask + kStages * 16;              // [2 wg][4 warps][8] f32
 constexpr uint32_t kOffRedSc = kOffRed + 2 * 4 * 8 * 4;            // [2 wg][4 warps][4] f32
-constexpr uint32_t kOffQf = kOffRedSc + 2 * 4 * 4 * 4;             // [16] f32: 2^-a per head
-constexpr uint32_t kOffOst = kOffQf + kHeads * 4;                  // [16 heads][512] bf16
-constexpr uint32_t kOffBar = kOffOst + kHeads * 512 * 2;
+constexpr uint32_t kOffQf = kOffRedSc + 2 * 4 * 4 * 4;             // [2][16] f32: 2^-a per head
+constexpr uint32_t kOffFac = kOffQf + 2 * kHeads * 4;             // [2 wg][8 alpha | 4 ratio] f32
+constexpr uint32_t kOffBar = kOffFac + 2 * 12 * 4;
 enum {
   kBarKvFull = 0,                   // [2] the tile, masks and scales of a block
   kBarKvEmpty = kBarKvFull + 2,     // [2]
@@ -115,6 +133,7 @@ enum {
   kBarODone,
   kBarOFinal,                       // one phase per unit: its last PV is done
   kBarQReady,                       // one phase per unit: Q' written
+  kBarQUsed,                        // one phase per unit: the softmax warps read qf_sh
   kBarDrain,                        // teardown: both MMA warps' MMAs are done
   kNumBars
 };
@@ -123,7 +142,8 @@ constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
 constexpr uint32_t kSmemBytes = kOffAbort + 4 + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzled operands need 1024-B alignment");
-static_assert(kOffRed % 16 == 0 && kOffOst % 16 == 0 && kOffBar % 8 == 0, "alignment");
+static_assert(kOffRed % 16 == 0 && kOffBar % 8 == 0, "alignment");
+static_assert(kHeads * 512 * 2 <= kPBytes, "O staging fits in P' region 1");
 
 struct Fp8Args {
   CUtensorMap kv_map;  // the cache as bytes [num_slots, row bytes], 128-byte boxes
@@ -176,6 +196,30 @@ __device__ __forceinline__ void split8(const float (&x)[8], uint2& hi, uint2& lo
   }
   hi = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
   lo = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
+}
+// Split p[0..7] * f into kTerms E4M3 terms, x = t0 + t1 / 16 (+ t2 / 256):
+// t0 = E4M3(x), each next term E4M3 of 16 times the residual left by the
+// one before (each residual and its product by 16 exact in f16; |x| <= 256
+// keeps every term within E4M3's range).  Term k's eight codes are stored
+// (x0 in the lowest byte) at dst(k) as each term is ready, so that only one
+// term's codes are live at a time.
+template <int kTerms, typename Dst>
+__device__ __forceinline__ void split_store8(const float (&p)[8], float f, Dst dst) {
+  const __half2 k16 = __float2half2_rn(16.f);
+  __half2 r[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) r[k] = __floats2half2_rn(p[2 * k] * f, p[2 * k + 1] * f);
+#pragma unroll
+  for (int t = 0; t < kTerms; ++t) {
+    uint32_t c[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) c[k] = e4m3x2_of_h2(r[k]);
+    *dst(t) = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+    if (t + 1 < kTerms) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) r[k] = __hmul2(__hsub2(r[k], h2_of_e4m3x2(c[k])), k16);
+    }
+  }
 }
 
 // Reduce v[0..7] (one value per head) over the 32 lanes of the warp; lane l
@@ -248,20 +292,102 @@ __device__ __forceinline__ void unit_range(const Fp8Args& a, int& u0, int& u1) {
   u1 = min(b < nbig ? u0 + a.upc : u0 + 1, a.n_units);
 }
 
+// Q' = the QK B operand of unit ui: rows [0, 16) = hi codes of heads
+// h0.., rows [16, 32) = lo codes, K-major, 128-byte chunks of 32 rows,
+// 128-byte swizzle; per head its factor 2^-a in buffer qbuf of qf_sh.  One
+// warp prepares heads hl0 and hl0 + 1 of the group.  For the 656-byte row the rope part of
+// Q stays bf16, in chunk 4 (16 rows x 128 bytes).
+template <bool kBf16Rope>
+__device__ __forceinline__ void prepare_q_pair(const FwdParams& p, uint8_t* sm,
+                                               const UnitInfo& ui, int hl0, int lane,
+                                               int qbuf) {
+  const bool rope = p.d_qk == 576;
+  float* qf_sh = reinterpret_cast<float*>(sm + kOffQf) + kHeads * qbuf;
+  const int n_fp8 = rope && !kBf16Rope ? 72 : 64;   // 8-channel pieces split to E4M3
+  const int n_pc = rope ? 72 : 64;
+  // both heads' loads first (one memory latency for the two)
+  uint4 x[2][3];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int hd = ui.h0 + hl0 + hh;
+    const bool live = hd < p.h;
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      const int k = lane + 32 * j;
+      x[hh][j] = (live && k < n_pc) ? __ldg(q_chunk(p, ui.t, hd, 8 * k))
+                                    : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int hl = hl0 + hh;
+    float mx = 0.f;
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      const int k = lane + 32 * j;
+      if (k < n_fp8) {
+        const uint32_t w[4] = {x[hh][j].x, x[hh][j].y, x[hh][j].z, x[hh][j].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[e] << 16)),
+                               fabsf(__uint_as_float(w[e] & 0xFFFF0000u))));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    // x * 2^ea in [128, 256) for the largest |x| (a zero row: ea = 0)
+    int ea = 0;
+    if (mx > 0.f) ea = 7 - (((__float_as_int(mx) >> 23) & 255) - 127);
+    ea = max(-126, min(126, ea));
+    const float up = pow2i(ea);
+    if (lane == 0) qf_sh[hl] = pow2i(-ea);
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      const int k = lane + 32 * j;
+      if (k < n_fp8) {
+        const uint32_t w[4] = {x[hh][j].x, x[hh][j].y, x[hh][j].z, x[hh][j].w};
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          f[2 * e] = __uint_as_float(w[e] << 16) * up;
+          f[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u) * up;
+        }
+        uint2 hi, lo;
+        split8(f, hi, lo);
+        const int byte = 8 * k;                         // channel = byte
+        const int cc = byte >> 7, u = (byte & 127) >> 4, off = byte & 8;
+        uint8_t* chunk = sm + kOffQ + cc * kQChunkBytes;
+        *reinterpret_cast<uint2*>(chunk + hl * 128 + (((u ^ (hl & 7)) << 4) | off)) = hi;
+        const int nl = 16 + hl;
+        *reinterpret_cast<uint2*>(chunk + nl * 128 + (((u ^ (nl & 7)) << 4) | off)) = lo;
+      } else if (kBf16Rope && k < n_pc) {
+        const int u = k - 64;                           // 16-byte unit of the bf16 row
+        *reinterpret_cast<uint4*>(sm + kOffQ + 4 * kQChunkBytes + hl * 128 +
+                                  ((u ^ (hl & 7)) << 4)) = x[hh][j];
+      }
+    }
+  }
+}
+
 // Each CTA runs its units (unit_range) in order.  Every role walks the same sequence of units and skips the
 // empty ones (no block), so that the CTA's running block count g (and the
 // running count of non-empty units) name the same barrier phases in every
 // role: block g uses stage g & 1 with phase (g >> 1) & 1, and the per-unit
-// barriers (Q ready, last PV done) have one phase per non-empty unit.  The
-// pipeline runs across unit boundaries: the producers load the next unit's
-// slot ids right after issuing the current unit's last gathers, and the
-// softmax warps write the next unit's Q' once the current unit's QK MMAs
-// are done (after its last scores were read), before its epilogue.
+// barriers (Q ready, Q used, last PV done) have one phase per non-empty
+// unit.  The pipeline runs across unit boundaries: the producers load the
+// next unit's slot ids right after issuing the current unit's last gathers,
+// issue its first block's gathers, and then write its Q' once the current
+// unit's last QK MMA has read Q' and the softmax warps have read the
+// current unit's Q factors, so that the next unit's first QK runs while the
+// softmax warps finish the current unit (its last block and epilogue).
 template <int kFmt>
 __global__ void __launch_bounds__(kThreads, 1)
 smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
   constexpr bool kGroup = kFmt != kE4m3;         // per-(slot, group) scales
   constexpr bool kBf16Rope = kFmt == kDsMla;     // rope stored as bf16 in the row
+  constexpr int kTerms = kGroup ? 3 : 2;         // E4M3 terms of a P' weight
+  constexpr int kNo = 16 * kTerms;               // PV N
+  constexpr uint32_t kColS = 4 * kNo;            // first S column
   extern __shared__ uint8_t smem_raw[];
   const FwdParams& p = a.p;
   const uint32_t raw = smem_u32(smem_raw);
@@ -289,7 +415,8 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
     mbar_init(bar(kBarPEmpty), 1);
     mbar_init(bar(kBarODone), 1);
     mbar_init(bar(kBarOFinal), 1);
-    mbar_init(bar(kBarQReady), kSoftmax);
+    mbar_init(bar(kBarQReady), kProducers);
+    mbar_init(bar(kBarQUsed), kSoftmax / 32);
     mbar_init(bar(kBarDrain), 2);
     *abort_flag = 0;
     fence_mbar_init_cluster();
@@ -370,7 +497,7 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
     W.drain(bar(kBarDrain), 0);
   } else if (warp == 13) {
     // ---- PV issuer ------------------------------------------------------
-    const uint32_t id_pv = idesc_e4m3(128, kNq, true, true);
+    const uint32_t id_pv = idesc_e4m3(128, kNo, true, true);
     const uint32_t pb = sb + kOffP;
     int g = 0;
     for (int u = u_begin; u < u_end; ++u) {
@@ -384,19 +511,19 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
         if (elect_one()) {
           fence_proxy_async_smem();
           // A = V^T of channel block c: chunk c (128 channels) x 32 keys,
-          // MN-major; B = P'^T: 32 keys x 32, MN-major (group scales: group
-          // c's 32 bytes of each key's row).  The unit's first block
-          // overwrites O (the softmax warps read the previous unit's O before
-          // they handed over this P').
+          // MN-major; B = P'^T: 32 keys x kNo, MN-major (group scales: group
+          // c's 48 bytes of each key's row, bytes 48 (c & 1) of region
+          // c >> 1).  The unit's first block overwrites O (the softmax warps
+          // read the previous unit's O before they handed over this P').
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
 #pragma unroll
             for (int ks = 0; ks < kBK / 32; ++ks) {
               const uint64_t ad =
                   sdesc(tile + c * kChunkBytes + ks * 4096, kChunkBytes, 1024, kLayoutSw128);
-              const uint64_t bd =
-                  sdesc(pb + ks * 4096 + (kGroup ? 32 * c : 0), kPBytes, 1024, kLayoutSw128);
-              mma_f8(tmem + kColO + 32u * (uint32_t)c, ad, bd, id_pv,
+              const uint32_t pc = kGroup ? (uint32_t)((c >> 1) * kPBytes + 48 * (c & 1)) : 0u;
+              const uint64_t bd = sdesc(pb + pc + ks * 4096, kPBytes, 1024, kLayoutSw128);
+              mma_f8(tmem + kColO + (uint32_t)(kNo * c), ad, bd, id_pv,
                      (j > 0 || ks > 0) ? 1u : 0u);
             }
           }
@@ -434,11 +561,14 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
     float* scs = reinterpret_cast<float*>(sm + kOffSc);
     uint32_t* masks = reinterpret_cast<uint32_t*>(sm + kOffMask);
     const uint32_t tx_bytes = (uint32_t)(8 * 4 * 512);
-    int g = 0, issued = 0;
+    int g = 0, issued = 0, ku = 0;
     bool stop = false;
-    for (int u = u_begin; u < u_end && !stop; ++u) {
+    for (int u = u_begin; u < u_end && !stop; ++u, ++ku) {
       const UnitInfo ui = unit_info(a, u);
-      if (ui.nb == 0) continue;
+      if (ui.nb == 0) {
+        --ku;
+        continue;
+      }
       // (the previous unit's gathers are all issued: the ids are free)
       named_bar_sync(1, kProducers);
       if (load_unit_slots(p, ui.t, ui.k0, ui.k1, ui.nb * kBK, slots, pt, kProducers))
@@ -477,6 +607,17 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
                      id < 0 ? 0u : 16u);
         }
         cp_async_arrive_noinc(full);
+        if (j == 0 && ku > 0) {
+          // Q' of this unit, once the softmax warps have read the previous
+          // unit's factors and its last QK (block g - 1) has read Q'
+          W.wait(bar(kBarQUsed), (ku - 1) & 1);
+          W.wait(bar(kBarSFull + ((g - 1) & 1)), ((g - 1) >> 1) & 1);
+          tc_fence_after();
+          prepare_q_pair<kBf16Rope>(p, sm, ui, 4 * wl, lane, ku & 1);
+          prepare_q_pair<kBf16Rope>(p, sm, ui, 4 * wl + 2, lane, ku & 1);
+          fence_proxy_async_smem();
+          mbar_arrive(bar(kBarQReady));
+        }
         // This thread's row: its valid bit and (group formats) its scales.
         const int id = bs[lane];
         const uint32_t m = __ballot_sync(0xffffffffu, id >= 0);
@@ -527,85 +668,13 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
     const uint32_t* masks = reinterpret_cast<const uint32_t*>(sm + kOffMask);
     float* red = reinterpret_cast<float*>(sm + kOffRed) + wg * 32;      // [4 warps][8]
     float* red_sc = reinterpret_cast<float*>(sm + kOffRedSc) + wg * 16; // [4 warps][4]
-    // This key's 128-byte row of the P' buffer (MN-major, 128-byte swizzle).
+    float* fac_sh = reinterpret_cast<float*>(sm + kOffFac) + wg * 12;   // the O rescale factors
+    // This key's 128-byte row of each P' region (MN-major, 128-byte swizzle).
     const uint32_t p_row = (uint32_t)(key >> 3) * 1024u + (uint32_t)(key & 7) * 128u;
     const uint32_t p_sw = (uint32_t)(key & 7);
     const float kscale = kFmt == kE4m3 ? __ldg(p.k_scale) : 1.f;
     const float rope_cs = a.scale_log2;                 // bf16 rope: not scaled by 2^-a
 
-    // Q' = the QK B operand of unit ui: rows [0, 16) = hi codes of heads
-    // h0.., rows [16, 32) = lo codes, K-major, 128-byte chunks of 32 rows,
-    // 128-byte swizzle.  Warp sw prepares heads 2 sw and 2 sw + 1.  For the
-    // 656-byte row the rope part of Q stays bf16, in chunk 4 (16 rows x 128
-    // bytes).  Ends with the arrival on Q ready.
-    auto prepare_q = [&](const UnitInfo& ui) {
-      const int n_fp8 = rope && !kBf16Rope ? 72 : 64;   // 8-channel pieces split to E4M3
-      const int n_pc = rope ? 72 : 64;
-      // both heads' loads first (one memory latency for the two)
-      uint4 x[2][3];
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int hd = ui.h0 + 2 * sw + hh;
-        const bool live = hd < p.h;
-#pragma unroll
-        for (int j = 0; j < 3; ++j) {
-          const int k = lane + 32 * j;
-          x[hh][j] = (live && k < n_pc) ? __ldg(q_chunk(p, ui.t, hd, 8 * k))
-                                        : make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int hl = 2 * sw + hh;
-        float mx = 0.f;
-#pragma unroll
-        for (int j = 0; j < 3; ++j) {
-          const int k = lane + 32 * j;
-          if (k < n_fp8) {
-            const uint32_t w[4] = {x[hh][j].x, x[hh][j].y, x[hh][j].z, x[hh][j].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[e] << 16)),
-                                   fabsf(__uint_as_float(w[e] & 0xFFFF0000u))));
-          }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        // x * 2^ea in [128, 256) for the largest |x| (a zero row: ea = 0)
-        int ea = 0;
-        if (mx > 0.f) ea = 7 - (((__float_as_int(mx) >> 23) & 255) - 127);
-        ea = max(-126, min(126, ea));
-        const float up = pow2i(ea);
-        if (lane == 0) qf_sh[hl] = pow2i(-ea);
-#pragma unroll
-        for (int j = 0; j < 3; ++j) {
-          const int k = lane + 32 * j;
-          if (k < n_fp8) {
-            const uint32_t w[4] = {x[hh][j].x, x[hh][j].y, x[hh][j].z, x[hh][j].w};
-            float f[8];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              f[2 * e] = __uint_as_float(w[e] << 16) * up;
-              f[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u) * up;
-            }
-            uint2 hi, lo;
-            split8(f, hi, lo);
-            const int byte = 8 * k;                         // channel = byte
-            const int cc = byte >> 7, u = (byte & 127) >> 4, off = byte & 8;
-            uint8_t* chunk = sm + kOffQ + cc * kQChunkBytes;
-            *reinterpret_cast<uint2*>(chunk + hl * 128 + (((u ^ (hl & 7)) << 4) | off)) = hi;
-            const int nl = 16 + hl;
-            *reinterpret_cast<uint2*>(chunk + nl * 128 + (((u ^ (nl & 7)) << 4) | off)) = lo;
-          } else if (kBf16Rope && k < n_pc) {
-            const int u = k - 64;                           // 16-byte unit of the bf16 row
-            *reinterpret_cast<uint4*>(sm + kOffQ + 4 * kQChunkBytes + hl * 128 +
-                                      ((u ^ (hl & 7)) << 4)) = x[hh][j];
-          }
-        }
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(bar(kBarQReady));
-    };
     // The next unit of this CTA with at least one block (u_end: none).
     auto next_unit = [&](int u) {
       for (++u; u < u_end; ++u)
@@ -653,21 +722,28 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
       write_empty(unit_info(a, u));
       ++u;
     }
-    if (u < u_end) prepare_q(unit_info(a, u));
+    if (u < u_end) {
+      // the first unit's Q' (the producer warps write the later ones)
+      prepare_q_pair<kBf16Rope>(p, sm, unit_info(a, u), 2 * sw, lane, 0);
+      fence_proxy_async_smem();
+      named_bar_sync(5, kSoftmax);
+      if (st < kProducers) mbar_arrive(bar(kBarQReady));
+    }
     while (u < u_end) {
       const UnitInfo ui = unit_info(a, u);
       const int un = next_unit(u);
       prefetch_q(un);
-      named_bar_sync(5, kSoftmax);                      // qf_sh of this unit written
-      // Per head of this warpgroup: Q factor 2^-a, folded with the score
-      // scale (and the per-tensor E4M3 scale).
-      float cs[8];
-      bool head_ok[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        cs[i] = qf_sh[8 * wg + i] * a.scale_log2 * kscale;
-        head_ok[i] = ui.h0 + 8 * wg + i < p.h;
-      }
+      W.wait(bar(kBarQReady), ku & 1);                  // qf_sh of this unit written
+      // Per head of this warpgroup: Q factor 2^-a (buffer ku & 1 of qf_sh,
+      // read where used), folded with the score scale (and the per-tensor
+      // E4M3 scale); heads i < n_live carry data.
+      const float* qf_u = qf_sh + kHeads * (ku & 1) + 8 * wg;
+      const float csc = a.scale_log2 * kscale;
+      const int n_live = p.h - ui.h0 - 8 * wg;
+      __syncwarp();
+      // (the producers write the other buffer next, then this one again
+      // once this warp has started the next unit)
+      if (lane == 0) mbar_arrive(bar(kBarQUsed));
       float m_run[8], l_part[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) { m_run[i] = -INFINITY; l_part[i] = 0.f; }
@@ -731,7 +807,7 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
                   acc[i] = fmaf(sc[4], fmaf(__uint_as_float(w[2][1][i]), 0.0625f,
                                             __uint_as_float(w[2][0][i])), acc[i]);
                 if (rope && kBf16Rope) r = __uint_as_float(w[2][0][i]);
-                sp[i] = fmaf(acc[i], cs[i], r * rope_cs);
+                sp[i] = fmaf(acc[i], qf_u[i] * csc, r * rope_cs);
               }
             }
           } else {
@@ -741,7 +817,8 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              sp[i] = fmaf(__uint_as_float(w1[i]), 0.0625f, __uint_as_float(w0[i])) * cs[i];
+              sp[i] = fmaf(__uint_as_float(w1[i]), 0.0625f, __uint_as_float(w0[i])) *
+                      (qf_u[i] * csc);
           }
         }
         tc_fence_before();
@@ -752,7 +829,7 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
         bool need = false;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          sp[i] = (key_ok && head_ok[i]) ? sp[i] : -INFINITY;
+          sp[i] = (key_ok && i < n_live) ? sp[i] : -INFINITY;
           need |= sp[i] > m_run[i] + kT;
         }
         if (kGroup) {
@@ -760,6 +837,7 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
           for (int gg = 0; gg < 4; ++gg) need |= R[gg] == 0.f || sc[gg] * R[gg] > 1.f;
         }
         float alpha[8], ratio[4] = {1.f, 1.f, 1.f, 1.f};
+        bool rescale = false;                       // some factor of O is not 1
 #pragma unroll
         for (int i = 0; i < 8; ++i) alpha[i] = 1.f;
         const bool voted = named_bar_or(2, kSoftmax, need);
@@ -800,6 +878,20 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
               }
             }
           }
+          // The warpgroup's O rescale factors (the same in all its threads)
+          // go to shared memory for the rescale below, so that they need not
+          // stay in registers; the barrier of the next block's vote orders
+          // their next write after every read.
+#pragma unroll
+          for (int i = 0; i < 8; ++i) rescale |= alpha[i] != 1.f;
+#pragma unroll
+          for (int gg = 0; gg < 4; ++gg) rescale |= ratio[gg] != 1.f;
+          if ((st & 127) == 0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) fac_sh[i] = alpha[i];
+#pragma unroll
+            for (int gg = 0; gg < 4; ++gg) fac_sh[8 + gg] = ratio[gg];
+          }
           named_bar_sync(nbar_wg, 128);             // red may be rewritten
         }
         float pe[8];
@@ -808,58 +900,53 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
           pe[i] = m_run[i] == -INFINITY ? 0.f : ex2_approx(sp[i] - m_run[i]);
           l_part[i] = fmaf(l_part[i], alpha[i], pe[i]);
         }
-        // a6 operand: P' hi / lo codes (per group with scales).
+        if (rescale && j >= 1) {                        // uniform in the warpgroup
+          // O^T row (channel `key` of each 128-channel block): this
+          // warpgroup's head columns (each term) *= alpha * ratio of the
+          // block.  (Rare: a lazy max step or a new group factor.)
+          W.wait(bar(kBarODone), (g - 1) & 1);
+          __syncwarp();
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            float fc[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) fc[i] = fac_sh[i] * fac_sh[8 + c];
+#pragma unroll 1
+            for (int part = 0; part < kTerms; ++part) {
+              const uint32_t col =
+                  tmem + lane_base + kColO + (uint32_t)(kNo * c) + 16u * part + 8u * wg;
+              uint32_t w[8];
+              tmem_ld8(col, w);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * fc[i]);
+              tmem_st8(col, w);
+            }
+          }
+          tmem_wait_st();
+        }
+        // a6 operand: P' codes.  Group scales: hi / mid / lo of group gg in
+        // region gg >> 1, 16-byte units 3 (gg & 1) + 0, 1, 2; one scale per
+        // tensor: hi / lo in units 0, 1 of region 0.
         if (g >= 1) W.wait(bar(kBarPEmpty), (g - 1) & 1);   // PV(g-1) read it
-        uint8_t* prow = sm + kOffP + p_row;
+        if (kGroup && j == 0 && ku > 0 && !p.fp32_out) {
+          // the previous unit's O copy has read the staging rows in region 1
+          if (st == 0) bulk_wait_read_all();
+          named_bar_sync(5, kSoftmax);
+        }
 #pragma unroll
         for (int gg = 0; gg < (kGroup ? 4 : 1); ++gg) {
-          const float f = kGroup ? sc[gg] * R[gg] * kPShift : kPShift;
-          float x[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) x[i] = pe[i] * f;
-          uint2 hi, lo;
-          split8(x, hi, lo);
-          *reinterpret_cast<uint2*>(prow + ((((uint32_t)(2 * gg) ^ p_sw) << 4) | (8u * wg))) = hi;
-          *reinterpret_cast<uint2*>(prow + ((((uint32_t)(2 * gg + 1) ^ p_sw) << 4) | (8u * wg))) =
-              lo;
+          uint8_t* prow = sm + kOffP + (uint32_t)(gg >> 1) * kPBytes + p_row;
+          split_store8<kTerms>(pe, kGroup ? sc[gg] * R[gg] * kPShift : kPShift, [&](int k) {
+            return reinterpret_cast<uint2*>(
+                prow + ((((uint32_t)(kTerms * (gg & 1) + k) ^ p_sw) << 4) | (8u * wg)));
+          });
         }
         fence_proxy_async_smem();
-        if (voted && j >= 1) {
-          // O^T row (channel `key` of each 128-channel block): this
-          // warpgroup's head columns (hi and lo) *= alpha * ratio of the block.
-          bool any = false;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) any |= alpha[i] != 1.f;
-#pragma unroll
-          for (int gg = 0; gg < 4; ++gg) any |= ratio[gg] != 1.f;
-          if (any) {                                      // uniform in the warpgroup
-            W.wait(bar(kBarODone), (g - 1) & 1);
-            __syncwarp();
-            tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-#pragma unroll
-              for (int part = 0; part < 2; ++part) {
-                const uint32_t col = tmem + lane_base + kColO + 32u * c + 16u * part + 8u * wg;
-                uint32_t w[8];
-                tmem_ld8(col, w);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                  w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha[i] * ratio[c]);
-                tmem_st8(col, w);
-              }
-            }
-            tmem_wait_st();
-          }
-        }
         tc_fence_before();
         mbar_arrive(bar(kBarPFull));
       }
-      // This unit's QK MMAs are done (its last scores were read): Q' of the
-      // next unit can be written now, so that its first QK runs during this
-      // unit's epilogue.
-      if (un < u_end) prepare_q(unit_info(a, un));
 
       // ---- a7: epilogue -------------------------------------------------------
       // Row sums: reduce the per-key partial sums over the block's keys.
@@ -875,30 +962,54 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) l_tot[i] = (red[i] + red[8 + i]) + (red[16 + i] + red[24 + i]);
       }
+      // Thread `key` < 8 writes the LSE of head 8 wg + key.
+      if (key < 8 && ui.h0 + 8 * wg + key < p.h) {
+        float mi = m_run[0], li = l_tot[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) {
+          mi = key == i ? m_run[i] : mi;
+          li = key == i ? l_tot[i] : li;
+        }
+        const bool empty = li == 0.f;         // (a NaN row sum is not empty)
+        const float lse_v = empty ? -INFINITY : (mi + log2f(li)) * 0.69314718055994530942f;
+        const int64_t orow = (int64_t)ui.t * p.h + ui.h0 + 8 * wg + key;
+        if (p.fp32_out)
+          p.lse_part[(int64_t)ui.split * p.T * p.h + orow] = lse_v;
+        else if (p.lse)
+          p.lse[orow] = lse_v;
+      }
       W.wait(bar(kBarOFinal), ku & 1);
       __syncwarp();
       tc_fence_after();
       const float oscale = kFmt == kE4m3 ? kscale : 1.f;
       float inv[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i)   // (fast division: the IEEE one costs ~125 cycles each here)
+      uint32_t live_l = 0u;                             // bit i: head i has a row sum
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {  // (fast division: the IEEE one costs ~125 cycles each here)
         inv[i] = l_tot[i] != 0.f ? __fdividef(oscale, l_tot[i] * kPShift) : 0.f;
+        live_l |= l_tot[i] != 0.f ? 1u << i : 0u;
+      }
       // bf16 O goes through the staging rows [16 heads][512] and leaves as
-      // one bulk copy (the token's rows of these heads are contiguous); the
-      // previous unit's copy has read the staging rows before they are
-      // rewritten.  fp32 partials are stored directly.
+      // one bulk copy (the token's rows of these heads are contiguous).  The
+      // rows are P' region 1: the unit's last PV has read it (O final); with
+      // group scales the previous unit's copy was waited for before this
+      // unit's first P' was written, with one scale per tensor P' does not
+      // use the region and the wait is here.  fp32 partials are stored
+      // directly.
       __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + kOffOst);
-      if (!p.fp32_out) {
+      if (!kGroup && !p.fp32_out) {
         if (st == 0) bulk_wait_read_all();
         named_bar_sync(5, kSoftmax);
       }
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
-        uint32_t wh[8], wl8[8];
+        uint32_t wh[8], wm[8], wl8[8];
         __syncwarp();
-        const uint32_t col = tmem + lane_base + kColO + 32u * c + 8u * wg;
+        const uint32_t col = tmem + lane_base + kColO + (uint32_t)(kNo * c) + 8u * wg;
         tmem_ld8(col, wh);
-        tmem_ld8(col + 16, wl8);
+        tmem_ld8(col + 16, wm);
+        if (kTerms == 3) tmem_ld8(col + 32, wl8);
         tmem_wait_ld();
         const float rc = kGroup ? R[c] : 1.f;
         // 1 / R_c: R_c is a power of two (or 0: no key of the unit has a
@@ -912,8 +1023,12 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
         for (int i = 0; i < 8; ++i) {
           // (no valid key for the head, or none with a nonzero scale in this
           // group: 0 exactly)
-          ov[i] = (l_tot[i] != 0.f && rinv > 0.f)
-                      ? fmaf(__uint_as_float(wl8[i]), 0.0625f, __uint_as_float(wh[i])) *
+          ov[i] = (((live_l >> i) & 1u) != 0u && rinv > 0.f)
+                      ? (kTerms == 3 ? fmaf(__uint_as_float(wl8[i]), 0.00390625f,
+                                            fmaf(__uint_as_float(wm[i]), 0.0625f,
+                                                 __uint_as_float(wh[i])))
+                                     : fmaf(__uint_as_float(wm[i]), 0.0625f,
+                                            __uint_as_float(wh[i]))) *
                             (inv[i] * rinv)
                       : 0.f;
         }
@@ -935,7 +1050,7 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
         } else {
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            if (head_ok[i]) {
+            if (i < n_live) {
               const int64_t orow = (int64_t)ui.t * p.h + ui.h0 + 8 * wg + i;
               p.o_part[((int64_t)ui.split * p.T * p.h + orow) * p.d_v + ch] = ov[i];
             }
@@ -953,22 +1068,6 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
                      sb + kOffOst, (uint32_t)(nh * 1024));
           bulk_commit_group();
         }
-      }
-      // Thread `key` < 8 writes the LSE of head 8 wg + key.
-      if (key < 8 && ui.h0 + 8 * wg + key < p.h) {
-        float mi = m_run[0], li = l_tot[0];
-#pragma unroll
-        for (int i = 1; i < 8; ++i) {
-          mi = key == i ? m_run[i] : mi;
-          li = key == i ? l_tot[i] : li;
-        }
-        const bool empty = li == 0.f;         // (a NaN row sum is not empty)
-        const float lse_v = empty ? -INFINITY : (mi + log2f(li)) * 0.69314718055994530942f;
-        const int64_t orow = (int64_t)ui.t * p.h + ui.h0 + 8 * wg + key;
-        if (p.fp32_out)
-          p.lse_part[(int64_t)ui.split * p.T * p.h + orow] = lse_v;
-        else if (p.lse)
-          p.lse[orow] = lse_v;
       }
       ++ku;
       // the empty units up to the next one with blocks
