@@ -554,7 +554,6 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
     const int wl = warp - 1;
     const int pt = tid - 32;
     constexpr int kRopePieces = kBf16Rope ? 8 : 4;
-    const int n_rp = rope ? kRopePieces : 0;           // 16-byte rope pieces a row
     const int row_bytes = kFmt == kDsMla ? kDsMlaRowBytes : p.d_qk;
     const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
     int* slots = reinterpret_cast<int*>(sm + kOffSlot);
@@ -586,25 +585,30 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
         const uint32_t full = bar(kBarKvFull + s);
         const uint32_t tile = sb + kOffTile + s * kStageBytes;
         const int* bs = slots + j * kBK + 32 * wl;
+        if (elect_one()) mbar_arrive_expect_tx(full, tx_bytes);
+        __syncwarp();
         if (elect_one()) {
-          mbar_arrive_expect_tx(full, tx_bytes);
           for (int q = 0; q < 8; ++q) {
-            const int y0 = bs[4 * q], y1 = bs[4 * q + 1], y2 = bs[4 * q + 2], y3 = bs[4 * q + 3];
+            const int4 y = *reinterpret_cast<const int4*>(bs + 4 * q);
 #pragma unroll
             for (int c = 0; c < 4; ++c)
               tma_gather4(tile + c * kChunkBytes + (32 * wl + 4 * q) * 128, &a.kv_map, 128 * c,
-                          y0, y1, y2, y3, full);
+                          y.x, y.y, y.z, y.w, full);
           }
         }
         __syncwarp();
-        for (int e = lane; e < 32 * n_rp; e += 32) {
-          const int r = e / n_rp, k = e - r * n_rp;      // row of the warp, rope piece
-          const int id = bs[r];
-          const int row = 32 * wl + r;
-          const uint32_t dst = tile + (uint32_t)(4 * kChunkBytes + row * 128) +
-                               ((uint32_t)(k ^ (row & 7)) << 4);
-          cp_async16(dst, kv8 + (size_t)(id < 0 ? 0 : id) * row_bytes + a.rope_x + 16 * k,
-                     id < 0 ? 0u : 16u);
+        if (rope) {
+#pragma unroll
+          for (int i = 0; i < kRopePieces; ++i) {
+            const int e = lane + 32 * i;
+            const int r = e / kRopePieces, k = e % kRopePieces;   // row of the warp, rope piece
+            const int id = bs[r];
+            const int row = 32 * wl + r;
+            const uint32_t dst = tile + (uint32_t)(4 * kChunkBytes + row * 128) +
+                                 ((uint32_t)(k ^ (row & 7)) << 4);
+            cp_async16(dst, kv8 + (size_t)(id < 0 ? 0 : id) * row_bytes + a.rope_x + 16 * k,
+                       id < 0 ? 0u : 16u);
+          }
         }
         cp_async_arrive_noinc(full);
         if (j == 0 && ku > 0) {
