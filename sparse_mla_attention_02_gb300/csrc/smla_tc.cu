@@ -96,8 +96,8 @@ constexpr int kMaxBlocks = 64;             // covers topk <= 3072 in one range
 constexpr uint32_t kOffSlot = kOffXs + kXBytes;                 // [blocks*48] i32
 constexpr uint32_t kOffMask = kOffSlot + kMaxBlocks * kBN * 4;  // [blocks][2] u32
 constexpr uint32_t kOffRed = kOffMask + kMaxBlocks * 8;         // [2][2][128] f32 half maxima
-constexpr uint32_t kOffL = kOffRed + 2 * 2 * 128 * 4;            // [2][128] f32 row sums
-constexpr uint32_t kOffBar = (kOffL + 2 * 128 * 4 + 7) & ~7u;
+constexpr uint32_t kOffL = kOffRed + 2 * 2 * 128 * 4;            // [2][2][128] f32 row sums
+constexpr uint32_t kOffBar = (kOffL + 2 * 2 * 128 * 4 + 7) & ~7u;
 enum {
   kBarKvFull = 0,
   kBarKvEmpty = kBarKvFull + kStages,
@@ -534,6 +534,7 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
     const float scale_log2 = a.scale_log2 * kscale;
     float m_run = -INFINITY;   // running max (log2 units), same in both warpgroups
     float l_run = 0.f;         // this warpgroup's running sum of exp2(s - m_run)
+    float lr_run = 0.f;        // the same sum of the bf16-rounded P (what PV multiplies)
     const uint32_t x_half = (uint32_t)wg * kXHalfBytes;
     const uint8_t* Xr = sm + kOffX + x_half;           // receive buffers (this half)
     const uint32_t x_peer = mapa(sb + kOffX + x_half, peer);
@@ -647,22 +648,24 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
         }
       }
       uint32_t pk[kBN / 4];
-      float lsum = 0.f;
+      float lsum = 0.f, lsum_r = 0.f;
       if (m_run == -INFINITY) {
 #pragma unroll
         for (int j = 0; j < kBN / 4; ++j) pk[j] = 0u;
       } else {
 #pragma unroll
         for (int j = 0; j < kBN / 2; j += 2) {
-          // The row sum uses the unrounded values (it sets the LSE); P goes
-          // to the PV MMA in bf16.
+          // P goes to the PV MMA in bf16; the row sum of the unrounded
+          // values sets the LSE, that of the rounded ones divides O.
           const float e0 = ex2_approx(fmaf(sp[j], cl, -m_run));
           const float e1 = ex2_approx(fmaf(sp[j + 1], cl, -m_run));
           pk[j / 2] = pack_bf16(e0, e1);
           lsum += e0 + e1;
+          lsum_r = add_bf16x2_f32(lsum_r, pk[j / 2]);
         }
       }
       l_run = l_run * alpha + lsum;
+      lr_run = lr_run * alpha + lsum_r;
       if (b >= 1) W.wait(bar(kBarPEmpty), (b - 1) & 1);   // PV(b-1) has read P
       // This half of the P row (24 bf16 = 3 chunks of 16 B, chunks 3 wg ..
       // 3 wg + 2) into the 128-byte-swizzled buffer.
@@ -683,10 +686,16 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
     // l = the two warpgroups' sums.  (A parity wait on the per-PV barrier
     // could pass a phase early when two PVs are still in flight; the final
     // barrier has exactly one phase.)
-    float* lsh = reinterpret_cast<float*>(sm + kOffL);  // [2][128]
+    // O is divided by the sum of the rounded P that PV multiplied, so that
+    // where one key carries a row its rounded weight cancels (the lazy
+    // running max leaves that weight anywhere in (1, 2^8], where bf16 is off
+    // by up to 2^-8 of it); the LSE takes the unrounded sum.
+    float* lsh = reinterpret_cast<float*>(sm + kOffL);  // [2 sums][2][128]
     lsh[wg * 128 + i] = l_run;
+    lsh[256 + wg * 128 + i] = lr_run;
     named_bar_sync(4, 256);
     const float l_tot = lsh[i] + lsh[128 + i];
+    const float lr_tot = lsh[256 + i] + lsh[384 + i];
     if (nb > 0) {
       W.wait(bar(kBarOFinal), 0);
       __syncwarp();
@@ -694,7 +703,7 @@ smla_tc_kernel(const __grid_constant__ TcArgs a) {
     }
     // empty: no valid key (a NaN row sum, from a NaN in the cache, is not)
     const bool empty = l_tot == 0.f || nb == 0;
-    const float inv = empty ? 0.f : __fdividef(kscale, l_tot);   // (IEEE division: slow here)
+    const float inv = empty ? 0.f : __fdividef(kscale, lr_tot);  // (IEEE division: slow here)
     const bool live = head < p.h;          // pad rows past h are not written
     const int64_t orow = (int64_t)t * p.h + (live ? head : 0);
     // Every lane of the warpgroup runs the TMEM loads (warp-collective);

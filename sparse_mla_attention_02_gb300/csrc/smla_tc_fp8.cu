@@ -12,23 +12,21 @@
 // E4M3 pair that carries bf16 precision:
 //   * Q (bf16): per head, x = q * 2^a with a power of two a that puts
 //     max|x| in [128, 256); hi = E4M3(x), lo = E4M3(16 (x - hi)), so that
-//     x = hi + lo / 16 up to 2^-8 of |x| (at least 2^-14 absolute).  The
+//     x = hi + lo / 16 up to 2^-9 of |x| (at least 2^-14 absolute).  The
 //     two are the MMA's N rows [16 heads hi | 16 heads lo]; the score is
 //     2^-a (S_hi + S_lo / 16), summed in fp32.
-//   * P (fp32, in [0, 2^4] by the lazy running max below): with group
-//     scales, each V group g gets x = p * scale_g * R_g * 2^4, R_g a power
-//     of two that keeps scale_g * R_g <= 1, split into three E4M3 terms,
-//     x = hi + mid / 16 + lo / 256 (mid = E4M3(16 (x - hi)), lo the same
-//     of the next residual), up to 2^-11 of |x| (the f16 step of the split)
-//     plus 2^-13.  Every key's weight carries its scale, so every key has
-//     this error, the heaviest one too; with two terms (2^-9) a row that
-//     one key carries with |v| near 4 came out 0.0208 from the oracle
-//     (the output's own bf16 rounding takes up to 0.0156 of the 2e-2 bound
-//     there).  The three are the 48 columns [hi | mid | lo] of the PV
-//     operand; O = (O_hi + O_mid / 16 + O_lo / 256) / (16 R_g l).  With one
-//     scale per tensor x = 16 p: the heaviest key's weight is exact (p = 1
-//     at the running max), as with a bf16 P, and two terms [hi | lo] (32
-//     columns) carry the others.
+//   * P (fp32, in [0, 2^4] by the lazy running max below): each V group g
+//     gets x = p * scale_g * R_g * 2^4, R_g a power of two that keeps
+//     scale_g * R_g <= 1 (one scale per tensor: x = 16 p), split into three
+//     E4M3 terms, x = hi + mid / 16 + lo / 256 (mid = E4M3(16 (x - hi)), lo
+//     the same of the next residual), up to 2^-11 of |x| (the f16 step of
+//     the split) plus 2^-13.  The weight of a key that carries its row can
+//     be anywhere in that range (it carries its scale, and the lazy max
+//     leaves p in (1, 2^4]), so it has this error; with two terms (2^-9) a
+//     row that one key carries with |v| near 4 came out 0.0208 from the
+//     oracle (the output's own bf16 rounding takes up to 0.0156 of the 2e-2
+//     bound there).  The three are the 48 columns [hi | mid | lo] of the PV
+//     operand; O = (O_hi + O_mid / 16 + O_lo / 256) / (16 R_g l).
 // Keys are the MMA's M dimension (keys-major), heads its N:
 //   S^T[keys, 32] = K[keys, d] . Q'^T[d, 32]      A = gathered tile, K-major
 //   O^T[ch, 48]  += V^T[ch, keys] . P'^T[keys, 48] A = the same tile, MN-major
@@ -87,7 +85,7 @@ constexpr int kHeads = 16;                 // heads per CTA
 constexpr int kNq = 32;                    // QK N: 16 heads hi | 16 heads lo
 constexpr int kQChunkBytes = kNq * 128;
 constexpr int kPBytes = kBK * 128;         // one P' region: a 128-byte row per key
-constexpr int kNoMax = 48;                 // PV N: 16 heads hi | mid | lo (group scales)
+constexpr int kNoMax = 48;                 // PV N: 16 heads hi | mid | lo
 constexpr int kThreads = 448;
 constexpr int kProducers = 128;            // warps 1..4
 constexpr int kSoftmax = 256;              // warps 5..12
@@ -385,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
   constexpr bool kGroup = kFmt != kE4m3;         // per-(slot, group) scales
   constexpr bool kBf16Rope = kFmt == kDsMla;     // rope stored as bf16 in the row
-  constexpr int kTerms = kGroup ? 3 : 2;         // E4M3 terms of a P' weight
+  constexpr int kTerms = 3;                      // E4M3 terms of a P' weight
   constexpr int kNo = 16 * kTerms;               // PV N
   constexpr uint32_t kColS = 4 * kNo;            // first S column
   extern __shared__ uint8_t smem_raw[];
@@ -930,9 +928,9 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
           }
           tmem_wait_st();
         }
-        // a6 operand: P' codes.  Group scales: hi / mid / lo of group gg in
-        // region gg >> 1, 16-byte units 3 (gg & 1) + 0, 1, 2; one scale per
-        // tensor: hi / lo in units 0, 1 of region 0.
+        // a6 operand: P' codes, hi / mid / lo of group gg in region gg >> 1,
+        // 16-byte units 3 (gg & 1) + 0, 1, 2 (one scale per tensor: one
+        // group, region 0).
         if (g >= 1) W.wait(bar(kBarPEmpty), (g - 1) & 1);   // PV(g-1) read it
         if (kGroup && j == 0 && ku > 0 && !p.fp32_out) {
           // the previous unit's O copy has read the staging rows in region 1
@@ -1013,7 +1011,7 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
         const uint32_t col = tmem + lane_base + kColO + (uint32_t)(kNo * c) + 8u * wg;
         tmem_ld8(col, wh);
         tmem_ld8(col + 16, wm);
-        if (kTerms == 3) tmem_ld8(col + 32, wl8);
+        tmem_ld8(col + 32, wl8);
         tmem_wait_ld();
         const float rc = kGroup ? R[c] : 1.f;
         // 1 / R_c: R_c is a power of two (or 0: no key of the unit has a
@@ -1028,11 +1026,8 @@ smla_tc_fp8_kernel(const __grid_constant__ Fp8Args a) {
           // (no valid key for the head, or none with a nonzero scale in this
           // group: 0 exactly)
           ov[i] = (((live_l >> i) & 1u) != 0u && rinv > 0.f)
-                      ? (kTerms == 3 ? fmaf(__uint_as_float(wl8[i]), 0.00390625f,
-                                            fmaf(__uint_as_float(wm[i]), 0.0625f,
-                                                 __uint_as_float(wh[i])))
-                                     : fmaf(__uint_as_float(wm[i]), 0.0625f,
-                                            __uint_as_float(wh[i]))) *
+                      ? fmaf(__uint_as_float(wl8[i]), 0.00390625f,
+                             fmaf(__uint_as_float(wm[i]), 0.0625f, __uint_as_float(wh[i]))) *
                             (inv[i] * rinv)
                       : 0.f;
         }

@@ -84,8 +84,8 @@ constexpr uint32_t kOffComb = kOffP + kPAreaBytes;                 // [2][128 ro
 constexpr uint32_t kOffSlot = kOffComb + 2 * kCombBytes;           // [blocks*64] i32
 constexpr uint32_t kOffMask = kOffSlot + kMaxBlocks * kBK * 4;     // [blocks][2] u32
 constexpr uint32_t kOffRed = kOffMask + kMaxBlocks * 8;            // [16 heads][4 warps] f32
-constexpr uint32_t kOffHead = kOffRed + kN * 4 * 4;                // [3][16] f32: alpha, l, m
-constexpr uint32_t kOffBar = kOffHead + 3 * kN * 4;
+constexpr uint32_t kOffHead = kOffRed + kN * 4 * 4;                // [4][16] f32: alpha, l, m, l~
+constexpr uint32_t kOffBar = kOffHead + 4 * kN * 4;
 enum {
   kBarKvFull = 0,                   // [2]
   kBarKvEmpty = kBarKvFull + 2,     // [2]
@@ -389,11 +389,16 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
       mbar_arrive(bar(kBarQReady));
     }
     const float scale_log2 = a.scale_log2;
-    float m_run[8], l_part[8];
+    // l_part: row sums of the unrounded P (they set the LSE); lr_part: of
+    // the bf16-rounded P that PV multiplies (they divide O, so that where
+    // one key carries a row its rounded weight cancels: the lazy running max
+    // leaves that weight anywhere in (1, 2^8], where bf16 is off by up to
+    // 2^-8 of it).
+    float m_run[8], l_part[8], lr_part[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) { m_run[i] = -INFINITY; l_part[i] = 0.f; }
+    for (int i = 0; i < 8; ++i) { m_run[i] = -INFINITY; l_part[i] = 0.f; lr_part[i] = 0.f; }
     float* red = reinterpret_cast<float*>(sm + kOffRed);   // [16 heads][4 warps]
-    float* hsh = reinterpret_cast<float*>(sm + kOffHead);  // [alpha | l | m][16 heads]
+    float* hsh = reinterpret_cast<float*>(sm + kOffHead);  // [alpha | l | m | l~][16 heads]
     // This key's 128-byte row in a P^T plane (MN-major, 128-byte swizzle):
     // atom key / 8, row key % 8, 16-byte chunk c at c ^ (key % 8).
     const uint32_t p_row = (uint32_t)(key >> 3) * 1024u + (uint32_t)(key & 7) * 128u;
@@ -476,10 +481,16 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
       float pe[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        // The row sums use the unrounded values (they set the LSE); P goes to
-        // the PV MMA in bf16.
         pe[i] = m_run[i] == -INFINITY ? 0.f : ex2_approx(sp[i] - m_run[i]);
         l_part[i] = fmaf(l_part[i], alpha[i], pe[i]);
+      }
+      uint32_t pk[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        pk[k] = pack_bf16(pe[2 * k], pe[2 * k + 1]);
+        lr_part[2 * k] = fmaf(lr_part[2 * k], alpha[2 * k], __uint_as_float(pk[k] << 16));
+        lr_part[2 * k + 1] =
+            fmaf(lr_part[2 * k + 1], alpha[2 * k + 1], __uint_as_float(pk[k] & 0xFFFF0000u));
       }
       // a6 operand: P^T into buffer b % kPBufs.
       const int pbi = b % kPBufs;
@@ -487,8 +498,7 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
       {
         uint8_t* prow = sm + kOffP + pbi * kPPlaneBytes + p_row;
         *reinterpret_cast<uint4*>(prow + (((uint32_t)hf ^ p_sw) << 4)) =
-            make_uint4(pack_bf16(pe[0], pe[1]), pack_bf16(pe[2], pe[3]),
-                       pack_bf16(pe[4], pe[5]), pack_bf16(pe[6], pe[7]));
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
       fence_proxy_async_smem();
       if (voted && b >= 1) {
@@ -543,6 +553,20 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
         }
       }
       named_bar_sync(4, kSoftmax);
+      // the same for the sums of the rounded P
+#pragma unroll
+      for (int i = 0; i < 8; ++i) l8[i] = lr_part[i];
+      const float wr = xreduce8<false>(l8, lane);
+      if ((lane & 17) == 0) red[(8 * hf + ((lane >> 1) & 7)) * 4 + q4] = wr;
+      named_bar_sync(4, kSoftmax);
+      if (key == 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 x = *reinterpret_cast<const float4*>(red + 4 * (8 * hf + i));
+          hsh[3 * kN + 8 * hf + i] = hf ? x.z + x.w : x.x + x.y;
+        }
+      }
+      named_bar_sync(4, kSoftmax);
     }
     if (nb > 0) {
       W.wait(bar(kBarOFinal), 0);
@@ -552,7 +576,7 @@ smla_tc_keys_kernel(const __grid_constant__ KeysArgs a) {
 #pragma unroll
     for (int hd = 0; hd < kN; ++hd) {
       const float l = hsh[kN + hd];
-      inv[hd] = (l == 0.f || nb == 0) ? 0.f : __fdividef(1.f, l);
+      inv[hd] = (l == 0.f || nb == 0) ? 0.f : __fdividef(1.f, hsh[3 * kN + hd]);
     }
 #pragma unroll
     for (int c = 0; c < 4; ++c) {

@@ -130,6 +130,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// acc + the two bf16 values packed in pk (low half first), each added as an
+// exact f32 value (PTX add.f32.bf16: one instruction per value).
+__device__ __forceinline__ float add_bf16x2_f32(float acc, uint32_t pk) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\t"
+      "add.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %0, h, %0;\n\t}"
+      : "+f"(acc) : "r"(pk));
+  return acc;
+}
+
 // The slot ids at top-k positions [k0, k0 + n) of one index row into
 // slots[0, n) (n a multiple of 4), -1 where masked: at or past k1, negative,
 // or >= num_slots (the last makes the return value true).  The nthr threads
