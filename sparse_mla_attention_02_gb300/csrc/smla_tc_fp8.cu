@@ -8,8 +8,8 @@
 // directly, half the bf16 HBM traffic, per-tensor k_scale or per-token x
 // 128-channel-group scales).  Here the gathered rows are not converted at
 // all: TMA gathers the raw E4M3 rows into shared memory, and both MMAs read
-// them as E4M3 operands.  The other operand of each product is split into an
-// E4M3 pair that carries bf16 precision:
+// them as E4M3 operands.  The other operand of each product is split into
+// E4M3 terms (a pair for Q, three for the softmax weights):
 //   * Q (bf16): per head, x = q * 2^a with a power of two a that puts
 //     max|x| in [128, 256); hi = E4M3(x), lo = E4M3(16 (x - hi)), so that
 //     x = hi + lo / 16 up to 2^-9 of |x| (at least 2^-14 absolute).  The
@@ -173,7 +173,7 @@ constexpr uint32_t idesc_e4m3(int M, int N, bool a_mn_major, bool b_mn_major) {
 
 // Split x0..x7 (|x| <= 448) into hi = E4M3(x) and lo = E4M3(16 (x - hi)),
 // eight codes each (x0 in the lowest byte).  The pairs go through f16: x is
-// rounded to f16 first (2^-11 relative, below the pair's 2^-8), and x - hi
+// rounded to f16 first (2^-11 relative, below the pair's 2^-9), and x - hi
 // and its product by 16 are exact in f16.
 __device__ __forceinline__ uint32_t e4m3x2_of_h2(__half2 h) {
   return (uint32_t)__nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&h),
