@@ -12,20 +12,21 @@
 // E4M3 terms (a pair for Q, three for the softmax weights):
 //   * Q (bf16): per head, x = q * 2^a with a power of two a that puts
 //     max|x| in [128, 256); hi = E4M3(x), lo = E4M3(16 (x - hi)), so that
-//     x = hi + lo / 16 up to 2^-9 of |x| (at least 2^-14 absolute).  The
+//     x = hi + lo / 16 up to 2^-9 of x's binade (or 2^-14 absolute).  The
 //     two are the MMA's N rows [16 heads hi | 16 heads lo]; the score is
 //     2^-a (S_hi + S_lo / 16), summed in fp32.
 //   * P (fp32, in [0, 2^4] by the lazy running max below): each V group g
 //     gets x = p * scale_g * R_g * 2^4, R_g a power of two that keeps
 //     scale_g * R_g <= 1 (one scale per tensor: x = 16 p), split into three
 //     E4M3 terms, x = hi + mid / 16 + lo / 256 (mid = E4M3(16 (x - hi)), lo
-//     the same of the next residual), up to 2^-11 of |x| (the f16 step of
-//     the split) plus 2^-13.  The weight of a key that carries its row can
-//     be anywhere in that range (it carries its scale, and the lazy max
-//     leaves p in (1, 2^4]), so it has this error; with two terms (2^-9) a
-//     row that one key carries with |v| near 4 came out 0.0208 from the
-//     oracle (the output's own bf16 rounding takes up to 0.0156 of the 2e-2
-//     bound there).  The three are the 48 columns [hi | mid | lo] of the PV
+//     the same of the next residual), which give back the f16 value of x
+//     exactly from 2^-6 up (below, to 2^-18 absolute): a weight keeps the
+//     f16 step of the split, 2^-11 of its binade.  The weight of a key that
+//     carries its row can be anywhere in that range (it carries its scale,
+//     and the lazy max leaves p in (1, 2^4]); with two terms (2^-9) a row
+//     that one key carries with |v| near 4 came out 0.0208 from the oracle
+//     (the output's own bf16 rounding takes up to 0.0156 of the 2e-2 bound
+//     there).  The three are the 48 columns [hi | mid | lo] of the PV
 //     operand; O = (O_hi + O_mid / 16 + O_lo / 256) / (16 R_g l).
 // Keys are the MMA's M dimension (keys-major), heads its N:
 //   S^T[keys, 32] = K[keys, d] . Q'^T[d, 32]      A = gathered tile, K-major
