@@ -29,6 +29,14 @@
  *  - Device-side conditions (an index >= num_slots, a bounded wait that ran
  *    out) never fault: the element is masked or the block exits, and a bit is
  *    set in a device status word that smla_get_device_status reads.
+ *  - Accuracy: O is bf16, LSE fp32.  Against the formula above evaluated in
+ *    fp64 on the same (dequantized) inputs, |dO| <= 2e-2 while |O| < 8 (the
+ *    bf16 rounding of O alone takes up to 2^-9 |O| there) and
+ *    |dLSE| <= 1e-3.  The softmax weights reach the PV product rounded to
+ *    bf16 (bf16 caches, O divided by the sum of the rounded weights) or as
+ *    three E4M3 terms that keep them to their f16 rounding (E4M3 caches), so
+ *    a row that one key carries keeps that key's V row to within the output's
+ *    own rounding.
  */
 #ifndef SMLA_H_
 #define SMLA_H_
