@@ -31,7 +31,7 @@
  *    set in a device status word that smla_get_device_status reads.
  *  - Accuracy: O is bf16, LSE fp32.  Against the formula above evaluated in
  *    fp64 on the same (dequantized) inputs, |dO| <= 2e-2 while |O| < 8 (the
- *    bf16 rounding of O alone takes up to 2^-9 |O| there) and
+ *    bf16 rounding of O alone takes up to 2^-8 |O| there) and
  *    |dLSE| <= 1e-3.  The softmax weights reach the PV product rounded to
  *    bf16 (bf16 caches, O divided by the sum of the rounded weights) or as
  *    three E4M3 terms that keep them to their f16 rounding (E4M3 caches), so
