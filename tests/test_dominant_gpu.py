@@ -19,51 +19,16 @@ range), which is asserted; and few tokens with 512-key rows, which the plan
 splits in two ranges whose partial outputs the combine merges (the late
 key at 400, in a later block of the second range).
 """
-import math
-
 import numpy as np
 import pytest
 import torch
 
 from sparse_mla_attention_02_gb300 import workloads as W
-from tests._helpers import oracle_fwd
+from tests._helpers import Guarded, oracle_fwd
+from tests._late_key import build, build_one_key
 from tests.test_parity_gpu import compare, gpu_fwd
 
 pytestmark = pytest.mark.gpu
-
-
-def build(kv_dtype, h, T, topk=256, late=200):
-    d_qk, S = 576, topk
-    sm_scale = 1.0 / math.sqrt(d_qk)
-    rng = np.random.default_rng(700 + 10 * kv_dtype + h)
-    g = np.linspace(0.5, 7.9, T * h).reshape(T, h)
-    rng.shuffle(g.reshape(-1))
-    a = g / (sm_scale * math.log2(math.e))
-    q = torch.zeros(T, h, d_qk, dtype=torch.bfloat16)
-    q[:, :, 0] = torch.from_numpy(a).to(torch.bfloat16)
-    # cache values (before quantization): channel 0 is the score channel
-    x = np.clip(rng.standard_normal((S, d_qk)), -3.0, 3.0)
-    x[:, 0] = -4.0
-    x[3::48, 0] = 1.0
-    x[late, 0] = 2.0
-    mags = np.array([4.375, 4.25, 4.125, 4.0])
-    x[late, 1:] = mags[rng.integers(0, 4, d_qk - 1)] * rng.choice([-1.0, 1.0], d_qk - 1)
-    xt = torch.from_numpy(x).float()
-    k_scale = None
-    if kv_dtype == W.KV_BF16:
-        kv = xt.to(torch.bfloat16)
-    elif kv_dtype == W.KV_FP8_E4M3:
-        kv = W.e4m3_bytes(xt / 0.05)
-        k_scale = torch.tensor([0.05], dtype=torch.float32)
-    else:
-        G = d_qk // 128 + (1 if d_qk % 128 else 0)
-        k_scale = torch.full((S, G), 0.05, dtype=torch.float32)
-        k_scale[late] = 0.0371                       # a scale that is not a power of two
-        kv = W.e4m3_bytes(xt / k_scale[:, torch.arange(d_qk) // 128])
-    idx = torch.arange(topk, dtype=torch.int32).repeat(T, 1)
-    valid = torch.full((T,), topk, dtype=torch.int32)
-    return W.Workload(f"dominant_kv{kv_dtype}_h{h}_T{T}", T, h, d_qk, 512, topk, S, kv_dtype,
-                      sm_scale, q, kv, k_scale, idx, valid, h)
 
 
 @pytest.mark.parametrize("kv_dtype,h,T", [
@@ -100,3 +65,31 @@ def test_late_dominant_key_split_rows(cuda_lib, kv_dtype, h, T):
     Or, Lr = oracle_fwd(w)
     assert np.abs(Or).max() > 4.0
     compare(O, L, Or, Lr, f"{w.name} ({plan['kernel']}, 2 ranges)")
+
+
+@pytest.mark.parametrize("kv_dtype,h", [
+    (W.KV_FP8_E4M3_GROUP128, 16),
+    (W.KV_FP8_E4M3_GROUP128, 128),
+    (W.KV_FP8_E4M3_GROUP4_KPE, 16),
+])
+def test_one_key_rows_at_the_worst_pair_scales(cuda_lib, kv_dtype, h):
+    """Rows of one key whose group scale puts its E4M3 weight where a pair of
+    E4M3 terms is furthest from it (2^-9), with V in [4, 8): two terms miss
+    the bound there (tests/test_softmax_rounding_cpu.py), the kernel's three
+    keep it."""
+    w = build_one_key(kv_dtype, h, 24)
+    wd = w.to("cuda")
+    if kv_dtype == W.KV_FP8_E4M3_GROUP4_KPE:
+        go = Guarded((w.T, w.h, w.d_v), torch.bfloat16)
+        gl = Guarded((w.T, w.h), torch.float32)
+        O, L = cuda_lib.smla_fwd_split_q(wd.q, None, wd.kv, wd.kv_dtype, wd.k_scale, wd.indices,
+                                         wd.valid_len, wd.sm_scale, kpe_scale=w.kpe_scale,
+                                         out=go.t, lse=gl.t, num_slots=w.num_slots)
+        torch.cuda.synchronize()
+        go.check(w.name)
+        gl.check(w.name)
+    else:
+        O, L = gpu_fwd(cuda_lib, wd)
+    Or, Lr = oracle_fwd(w)
+    assert np.abs(Or).max() > 4.0
+    compare(O, L, Or, Lr, w.name)
